@@ -71,9 +71,9 @@ def _declare(lib):
     lib.svo_residual.restype = ctypes.c_double
     lib.svo_icdf.argtypes = [_P, ctypes.c_int, ctypes.c_double, _P]
     lib.svo_icdf.restype = ctypes.c_int
-    lib.svo_verify_chain.argtypes = [ctypes.c_int] * 4 + [_P] * 7 + [_P] * 7
+    lib.svo_verify_chain.argtypes = [ctypes.c_int] * 4 + [_P] * 7 + [_P] * 8
     lib.svo_verify_chain.restype = ctypes.c_int
-    lib.svo_verify_tree.argtypes = [ctypes.c_int] * 6 + [_P] * 10 + [_P] * 6
+    lib.svo_verify_tree.argtypes = [ctypes.c_int] * 6 + [_P] * 10 + [_P] * 7
     lib.svo_verify_tree.restype = ctypes.c_int
     return lib
 
@@ -153,12 +153,15 @@ def verify_chain(target, draft, tokens, temperature, uniforms,
     tk = None if top_k is None else np.ascontiguousarray(top_k, dtype=np.int32)
     out = dict(out_tokens=np.zeros((B, K + 1), np.int32), out_len=np.zeros(B, np.int32),
                accept_len=np.zeros(B, np.int32), p_at=np.zeros((B, K)),
-               q_at=np.zeros((B, K)), margin=np.zeros(B), status=np.zeros(B, np.int32))
+               q_at=np.zeros((B, K)), margin_accept=np.zeros(B), margin_draw=np.zeros(B),
+               status=np.zeros(B, np.int32))
     lib.svo_verify_chain(B, K, V, dt, _ptr(target), _ptr(draft), _ptr(tokens), _ptr(nd),
                          _ptr(temperature), _ptr(tk), _ptr(uniforms),
                          _ptr(out["out_tokens"]), _ptr(out["out_len"]),
                          _ptr(out["accept_len"]), _ptr(out["p_at"]), _ptr(out["q_at"]),
-                         _ptr(out["margin"]), _ptr(out["status"]))
+                         _ptr(out["margin_accept"]), _ptr(out["margin_draw"]),
+                         _ptr(out["status"]))
+    out["margin"] = np.minimum(out["margin_accept"], out["margin_draw"])
     return out
 
 
@@ -196,13 +199,16 @@ def verify_tree(target, draft, node_tokens, parent, q_row, temperature,
     out = dict(out_tokens=np.zeros((B, max_depth + 1), np.int32),
                out_len=np.zeros(B, np.int32), accept_len=np.zeros(B, np.int32),
                accepted_nodes=np.zeros((B, max(max_depth, 1)), np.int32),
-               margin=np.zeros(B), status=np.zeros(B, np.int32))
+               margin_accept=np.zeros(B), margin_draw=np.zeros(B),
+               status=np.zeros(B, np.int32))
     lib.svo_verify_tree(B, N, M, V, dt, max_depth, _ptr(target), _ptr(draft),
                         _ptr(node_tokens), _ptr(parent), _ptr(q_row), _ptr(nn),
                         _ptr(temperature), _ptr(tk), _ptr(u_accept), _ptr(u_sample),
                         _ptr(out["out_tokens"]), _ptr(out["out_len"]),
                         _ptr(out["accept_len"]), _ptr(out["accepted_nodes"]),
-                        _ptr(out["margin"]), _ptr(out["status"]))
+                        _ptr(out["margin_accept"]), _ptr(out["margin_draw"]),
+                        _ptr(out["status"]))
+    out["margin"] = np.minimum(out["margin_accept"], out["margin_draw"])
     if max_depth == 0:
         out["accepted_nodes"] = out["accepted_nodes"][:, :0]
     return out

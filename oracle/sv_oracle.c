@@ -229,15 +229,17 @@ static double accept_margin(double u, double q, double p) {
  * accept_len [B] = accepted drafts = KV truncation index,
  * p_at / q_at [B][K] = p_i(x_i), q_i(x_i) for every i < num_drafts (NaN
  * elsewhere; q_at is NaN for greedy requests, whose draft rows are unused),
- * margin [B] = smallest relative distance of any decision taken to its
- * boundary (+inf when every decision is exact), status [B].
+ * margin_accept [B] = smallest relative distance |u q - p| / q of an accept
+ * test taken to its boundary, margin_draw [B] = the inverse-CDF margin of the
+ * final draw (+inf where the decisions are exact, e.g. greedy), status [B].
  */
 int svo_verify_chain(int B, int K, int V, int dtype, const void* target,
                      const void* draft, const int* tokens,
                      const int* num_drafts, const float* temperature,
                      const int* top_k, const float* uniforms, int* out_tokens,
                      int* out_len, int* accept_len, double* p_at,
-                     double* q_at, double* margin, int* status) {
+                     double* q_at, double* margin_accept, double* margin_draw,
+                     int* status) {
   const size_t es = dtype == 0 ? 2 : 4;
   double* p = (double*)malloc(sizeof(double) * (size_t)V);
   double* q = (double*)malloc(sizeof(double) * (size_t)V);
@@ -260,7 +262,8 @@ int svo_verify_chain(int B, int K, int V, int dtype, const void* target,
     }
     out_len[b] = 0;
     accept_len[b] = 0;
-    margin[b] = INFINITY;
+    margin_accept[b] = INFINITY;
+    margin_draw[b] = INFINITY;
     status[b] = SVO_OK;
 
     int st = SVO_OK;
@@ -300,7 +303,7 @@ int svo_verify_chain(int B, int K, int V, int dtype, const void* target,
         while (n < nd) {
           double pi = p_at[(size_t)b * K + n], qi = q_at[(size_t)b * K + n];
           double mg = accept_margin((double)u[n], qi, pi);
-          if (mg < margin[b]) margin[b] = mg;
+          if (mg < margin_accept[b]) margin_accept[b] = mg;
           if ((double)u[n] * qi < pi) ++n;
           else break;
         }
@@ -318,7 +321,7 @@ int svo_verify_chain(int B, int K, int V, int dtype, const void* target,
           /* all drafts accepted: bonus token from p_{nd+1} */
           token = svo_icdf(p, V, (double)u[K], &mg);
         }
-        if (mg < margin[b]) margin[b] = mg;
+        margin_draw[b] = mg;
         if (st == SVO_OK && token < 0) st = SVO_EMASS;
       }
       if (st != SVO_OK) { status[b] = st; ++n_err; continue; }
@@ -355,7 +358,8 @@ int svo_verify_chain(int B, int K, int V, int dtype, const void* target,
  * Greedy: go to the first child whose token is argmax p_node, else emit it.
  *
  * Outputs: out_tokens [B][max_depth+1], accepted_nodes [B][max_depth]
- * (-1 padded), out_len, accept_len, margin, status as for the chain.
+ * (-1 padded), out_len, accept_len, margin_accept, margin_draw, status as
+ * for the chain.
  */
 int svo_verify_tree(int B, int N, int M, int V, int dtype, int max_depth,
                     const void* target, const void* draft,
@@ -364,7 +368,8 @@ int svo_verify_tree(int B, int N, int M, int V, int dtype, int max_depth,
                     const float* temperature, const int* top_k,
                     const float* u_accept, const float* u_sample,
                     int* out_tokens, int* out_len, int* accept_len,
-                    int* accepted_nodes, double* margin, int* status) {
+                    int* accepted_nodes, double* margin_accept,
+                    double* margin_draw, int* status) {
   const size_t es = dtype == 0 ? 2 : 4;
   double* p = (double*)malloc(sizeof(double) * (size_t)V);
   double* r = (double*)malloc(sizeof(double) * (size_t)V);
@@ -388,7 +393,8 @@ int svo_verify_tree(int B, int N, int M, int V, int dtype, int max_depth,
     for (int i = 0; i < max_depth; ++i) acc[i] = -1;
     out_len[b] = 0;
     accept_len[b] = 0;
-    margin[b] = INFINITY;
+    margin_accept[b] = INFINITY;
+    margin_draw[b] = INFINITY;
     status[b] = SVO_OK;
 
     int st = SVO_OK;
@@ -427,7 +433,7 @@ int svo_verify_tree(int B, int N, int M, int V, int dtype, int max_depth,
       double mg = INFINITY;
       if (!has_child) { /* leaf: bonus token from p_node */
         token = svo_icdf(p, V, (double)u_sample[b], &mg);
-        if (mg < margin[b]) margin[b] = mg;
+        margin_draw[b] = mg;
         break;
       }
       memcpy(r, p, sizeof(double) * (size_t)V);
@@ -438,7 +444,7 @@ int svo_verify_tree(int B, int N, int M, int V, int dtype, int max_depth,
         if (st != SVO_OK) break;
         int xc = tok[c];
         double m1 = accept_margin((double)ua[c], q[xc], r[xc]);
-        if (m1 < margin[b]) margin[b] = m1;
+        if (m1 < margin_accept[b]) margin_accept[b] = m1;
         if ((double)ua[c] * q[xc] < r[xc]) { next = c; break; }
         double S = svo_residual(r, q, V, w);
         if (S > 0.0)
@@ -453,7 +459,7 @@ int svo_verify_tree(int B, int N, int M, int V, int dtype, int max_depth,
         continue;
       }
       token = svo_icdf(r, V, (double)u_sample[b], &mg);
-      if (mg < margin[b]) margin[b] = mg;
+      margin_draw[b] = mg;
       break;
     }
     if (st == SVO_OK && token < 0) st = SVO_EMASS;

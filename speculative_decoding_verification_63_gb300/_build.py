@@ -1,0 +1,43 @@
+"""Build of libspecverify.so with nvcc for sm_103a (GB300), in-tree."""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+LIBRARY = os.path.join(PKG, "libspecverify.so")
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def sources() -> list[str]:
+    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC)
+                  if f.endswith((".cu", ".cuh")))
+
+
+def nvcc() -> str:
+    for cand in (shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found: the CUDA 13 toolkit is required to build libspecverify")
+
+
+def build_library(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+    """Compile csrc/specverify.cu into libspecverify.so (one translation
+    unit, -O3, IEEE division and sqrt, no fast-math)."""
+    newest = max(os.path.getmtime(p) for p in sources() + [os.path.join(INCLUDE, "specverify.h")])
+    if not force and os.path.exists(LIBRARY) and os.path.getmtime(LIBRARY) >= newest:
+        return LIBRARY
+    tmp = LIBRARY + f".tmp{os.getpid()}"
+    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
+           "-cudart", "shared", "-Xlinker", "-rpath,/usr/local/cuda/lib64",
+           f"-I{INCLUDE}", "-o", tmp, os.path.join(CSRC, "specverify.cu"), *extra_flags]
+    if verbose:
+        cmd.insert(1, "-Xptxas=-v")
+        print(" ".join(cmd))
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, LIBRARY)
+    return LIBRARY

@@ -1,0 +1,319 @@
+// specverify.cu -- C ABI of libspecverify (see include/specverify.h):
+// argument checks, workspace layout, launch of the sm_103a kernels.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "specverify.h"
+#include "sv_chain.cuh"
+#include "sv_tree.cuh"
+
+namespace {
+
+using namespace sv;
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+struct Layout {
+  size_t tickets, partials, scratch, total;
+};
+
+// The header and the per-request tickets sit at fixed offsets with a fixed
+// capacity (SV_MAX_B), so the region that every call leaves zeroed is the
+// same for all problem sizes: one initialised workspace serves chain and
+// tree calls of any shape, one call at a time.
+Layout layout_for(int64_t /*B*/, int64_t rows_max, int64_t ipr, int64_t scratch_floats) {
+  Layout L;
+  L.tickets = align_up(sizeof(WsHeader));
+  L.partials = align_up(L.tickets + sizeof(unsigned int) * static_cast<size_t>(SV_MAX_B));
+  L.scratch = align_up(L.partials + sizeof(float2) * static_cast<size_t>(rows_max * ipr));
+  L.total = align_up(L.scratch + sizeof(float) * static_cast<size_t>(scratch_floats));
+  return L;
+}
+
+Ws ws_view(void* base, const Layout& L) {
+  char* p = static_cast<char*>(base);
+  Ws w;
+  w.hdr = reinterpret_cast<WsHeader*>(p);
+  w.tickets = reinterpret_cast<unsigned int*>(p + L.tickets);
+  w.partials = reinterpret_cast<float2*>(p + L.partials);
+  w.scratch = reinterpret_cast<float*>(p + L.scratch);
+  return w;
+}
+
+int es_of(sv_dtype d) { return d == SV_BF16 ? 2 : 4; }
+int chunk_el_of(sv_dtype d) { return kChunkBytes / es_of(d); }
+
+// Per-device facts, looked up once.
+struct DeviceInfo {
+  int sms = 0;
+  bool supported = false;
+};
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+bool g_known[64];
+
+sv_status device_info(DeviceInfo& out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ECUDA;
+  if (dev < 0 || dev >= 64) return SV_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_known[dev]) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return SV_ECUDA;
+    g_dev[dev].sms = sms;
+    g_dev[dev].supported = (major == 10 && minor == 3);
+    g_known[dev] = true;
+  }
+  out = g_dev[dev];
+  return out.supported ? SV_OK : SV_EUNSUPPORTED;
+}
+
+size_t pos_table_bytes(int n_req, bool aux) {
+  return (sizeof(float2) + (aux ? 8 : 0)) * n_req + sizeof(int) * n_req +
+         sizeof(int) * (n_req + 1);
+}
+
+template <class P>
+size_t kernel_smem(int n_req) {
+  return static_cast<size_t>(kStages) * kChunkBytes + ((sizeof(Shared) + 15) & ~size_t(15)) +
+         pos_table_bytes(n_req, P::kAux);
+}
+
+template <class P>
+sv_status launch(const P& prob, int grid, cudaStream_t stream) {
+  const size_t smem = kernel_smem<P>(prob.n_req);
+  if (cudaFuncSetAttribute(verify_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return SV_ECUDA;
+  verify_kernel<P><<<grid, kThreads, smem, stream>>>(prob);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
+    return SV_EUNSUPPORTED;
+  return e == cudaSuccess ? SV_OK : SV_ECUDA;
+}
+
+bool bulk_ok(const void* base, int64_t stride_bytes, int64_t row_bytes) {
+  return base != nullptr && (reinterpret_cast<uintptr_t>(base) & 15) == 0 &&
+         (stride_bytes & 15) == 0 && (row_bytes & 15) == 0;
+}
+
+__global__ void wait_selftest_kernel(WsHeader* hdr, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // nothing ever arrives: the bounded wait must give up and report
+    if (!mbar_wait_bounded(&bar, 0, limit_ns)) record_error(&hdr->error, SV_DERR_TIMEOUT);
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t sv_version(void) { return 100; }
+
+const char* sv_status_string(sv_status s) {
+  switch (s) {
+    case SV_OK: return "SV_OK";
+    case SV_EINVAL: return "SV_EINVAL: invalid argument";
+    case SV_ECUDA: return "SV_ECUDA: CUDA runtime error";
+    case SV_ETIMEOUT: return "SV_ETIMEOUT: a bounded device wait expired";
+    case SV_EDATA: return "SV_EDATA: input data broke a precondition";
+    case SV_EWORKSPACE: return "SV_EWORKSPACE: workspace missing, too small or misaligned";
+    case SV_EUNSUPPORTED: return "SV_EUNSUPPORTED: needs an sm_103 (GB300) device";
+  }
+  return "unknown sv_status";
+}
+
+size_t sv_chain_workspace_bytes(int32_t B, int32_t K, int32_t V, sv_dtype dtype,
+                                int32_t max_top_k) {
+  if (B < 0 || B > SV_MAX_B || K < 0 || K > SV_MAX_K || V < 1 || V > SV_MAX_V ||
+      (dtype != SV_BF16 && dtype != SV_FP32) || max_top_k < 0 || max_top_k > SV_MAX_TOPK)
+    return 0;
+  const int64_t ipr = (V + chunk_el_of(dtype) - 1) / chunk_el_of(dtype);
+  return layout_for(B, static_cast<int64_t>(B) * (2 * K + 1), ipr, 0).total;
+}
+
+size_t sv_tree_workspace_bytes(int32_t B, int32_t N, int32_t M, int32_t V, sv_dtype dtype,
+                               int32_t max_top_k) {
+  if (B < 0 || B > SV_MAX_TREE_B || N < 1 || N > SV_MAX_TREE_NODES || M < 1 ||
+      M > SV_MAX_TREE_NODES || V < 1 || V > SV_MAX_V || (dtype != SV_BF16 && dtype != SV_FP32) ||
+      max_top_k < 0 || max_top_k > SV_MAX_TOPK)
+    return 0;
+  const int64_t ipr = (V + chunk_el_of(dtype) - 1) / chunk_el_of(dtype);
+  return layout_for(B, static_cast<int64_t>(B) * (N + M), ipr, static_cast<int64_t>(B) * 2 * V)
+      .total;
+}
+
+sv_status sv_workspace_init(void* workspace, size_t ws_bytes, sv_stream_t stream) {
+  if (workspace == nullptr || ws_bytes < sizeof(WsHeader)) return SV_EWORKSPACE;
+  return cudaMemsetAsync(workspace, 0, ws_bytes, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? SV_OK
+             : SV_ECUDA;
+}
+
+sv_status sv_verify_chain(const sv_chain_args* a, void* workspace, size_t ws_bytes,
+                          sv_stream_t stream) {
+  if (a == nullptr) return SV_EINVAL;
+  if (a->B < 0 || a->B > SV_MAX_B || a->K < 0 || a->K > SV_MAX_K || a->V < 1 ||
+      a->V > SV_MAX_V || (a->dtype != SV_BF16 && a->dtype != SV_FP32) || a->max_top_k < 0 ||
+      a->max_top_k > SV_MAX_TOPK)
+    return SV_EINVAL;
+  if (a->B == 0) return SV_OK;
+  if (a->target_logits == nullptr || a->target_row_stride < a->V ||
+      (a->draft_tokens == nullptr && a->K > 0) ||
+      a->temperature == nullptr || a->uniforms == nullptr || a->out_tokens == nullptr ||
+      a->out_len == nullptr || a->accept_len == nullptr)
+    return SV_EINVAL;
+  if (a->draft_logits != nullptr && a->draft_row_stride < a->V) return SV_EINVAL;
+  const size_t need = sv_chain_workspace_bytes(a->B, a->K, a->V, a->dtype, a->max_top_k);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0 ||
+      ws_bytes < need)
+    return SV_EWORKSPACE;
+  DeviceInfo dev;
+  const sv_status ds = device_info(dev);
+  if (ds != SV_OK) return ds;
+
+  const int es = es_of(a->dtype);
+  const int chunk_el = chunk_el_of(a->dtype);
+  const int ipr = (a->V + chunk_el - 1) / chunk_el;
+  const Layout L = layout_for(a->B, static_cast<int64_t>(a->B) * (2 * a->K + 1), ipr, 0);
+
+  ChainProblem p;
+  p.n_req = a->B;
+  p.K = a->K;
+  p.V = a->V;
+  p.es = es;
+  p.ipr = ipr;
+  p.chunk_el = chunk_el;
+  p.max_topk = a->max_top_k;
+  p.target = static_cast<const char*>(a->target_logits);
+  p.t_stride = a->target_row_stride * es;
+  p.draft = static_cast<const char*>(a->draft_logits);
+  p.d_stride = a->draft_logits ? a->draft_row_stride * es : 0;
+  p.bulk = bulk_ok(a->target_logits, p.t_stride, static_cast<int64_t>(a->V) * es) &&
+           (a->draft_logits == nullptr ||
+            bulk_ok(a->draft_logits, p.d_stride, static_cast<int64_t>(a->V) * es));
+  p.tokens = a->draft_tokens;
+  p.num_drafts = a->num_drafts;
+  p.temperature = a->temperature;
+  p.top_k = a->top_k;
+  p.uniforms = a->uniforms;
+  p.out_tokens = a->out_tokens;
+  p.out_len = a->out_len;
+  p.accept_len = a->accept_len;
+  p.p_at = a->p_at_draft;
+  p.q_at = a->q_at_draft;
+  p.ws = ws_view(workspace, L);
+
+  const int64_t items_max = static_cast<int64_t>(a->B) * (2 * a->K + 1) * ipr;
+  const int grid = static_cast<int>(items_max < dev.sms ? (items_max < 1 ? 1 : items_max) : dev.sms);
+  return launch(p, grid, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sv_status sv_verify_tree(const sv_tree_args* a, void* workspace, size_t ws_bytes,
+                         sv_stream_t stream) {
+  if (a == nullptr) return SV_EINVAL;
+  if (a->B < 0 || a->B > SV_MAX_TREE_B || a->N < 1 || a->N > SV_MAX_TREE_NODES || a->M < 1 ||
+      a->M > SV_MAX_TREE_NODES || a->V < 1 || a->V > SV_MAX_V || a->max_depth < 0 ||
+      a->max_depth >= a->N || (a->dtype != SV_BF16 && a->dtype != SV_FP32) ||
+      a->mode != SV_TREE_MSS || a->max_top_k < 0 || a->max_top_k > SV_MAX_TOPK)
+    return SV_EINVAL;
+  if (a->B == 0) return SV_OK;
+  if (a->target_logits == nullptr || a->target_row_stride < a->V || a->node_tokens == nullptr ||
+      a->parent == nullptr || a->q_row == nullptr || a->temperature == nullptr ||
+      a->u_accept == nullptr || a->u_sample == nullptr || a->out_tokens == nullptr ||
+      a->out_len == nullptr || a->accept_len == nullptr || a->accepted_nodes == nullptr)
+    return SV_EINVAL;
+  if (a->draft_logits != nullptr && a->draft_row_stride < a->V) return SV_EINVAL;
+  const size_t need = sv_tree_workspace_bytes(a->B, a->N, a->M, a->V, a->dtype, a->max_top_k);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0 ||
+      ws_bytes < need)
+    return SV_EWORKSPACE;
+  DeviceInfo dev;
+  const sv_status ds = device_info(dev);
+  if (ds != SV_OK) return ds;
+
+  const int es = es_of(a->dtype);
+  const int chunk_el = chunk_el_of(a->dtype);
+  const int ipr = (a->V + chunk_el - 1) / chunk_el;
+  const Layout L = layout_for(a->B, static_cast<int64_t>(a->B) * (a->N + a->M), ipr,
+                              static_cast<int64_t>(a->B) * 2 * a->V);
+  TreeProblem p;
+  p.n_req = a->B;
+  p.N = a->N;
+  p.M = a->M;
+  p.V = a->V;
+  p.max_depth = a->max_depth;
+  p.es = es;
+  p.ipr = ipr;
+  p.chunk_el = chunk_el;
+  p.max_topk = a->max_top_k;
+  p.target = static_cast<const char*>(a->target_logits);
+  p.t_stride = a->target_row_stride * es;
+  p.draft = static_cast<const char*>(a->draft_logits);
+  p.d_stride = a->draft_logits ? a->draft_row_stride * es : 0;
+  p.bulk = bulk_ok(a->target_logits, p.t_stride, static_cast<int64_t>(a->V) * es) &&
+           (a->draft_logits == nullptr ||
+            bulk_ok(a->draft_logits, p.d_stride, static_cast<int64_t>(a->V) * es));
+  p.tokens = a->node_tokens;
+  p.parent = a->parent;
+  p.q_row = a->q_row;
+  p.num_nodes = a->num_nodes;
+  p.temperature = a->temperature;
+  p.top_k = a->top_k;
+  p.u_accept = a->u_accept;
+  p.u_sample = a->u_sample;
+  p.out_tokens = a->out_tokens;
+  p.out_len = a->out_len;
+  p.accept_len = a->accept_len;
+  p.accepted_nodes = a->accepted_nodes;
+  p.ws = ws_view(workspace, L);
+
+  const int64_t items_max = static_cast<int64_t>(a->B) * (a->N + a->M) * ipr;
+  const int grid = static_cast<int>(items_max < dev.sms ? (items_max < 1 ? 1 : items_max) : dev.sms);
+  return launch(p, grid, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sv_status sv_get_error(void* workspace, sv_stream_t stream, int32_t* device_flags) {
+  if (workspace == nullptr) return SV_EWORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SV_ECUDA;
+  WsHeader h;
+  if (cudaMemcpy(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return SV_ECUDA;
+  const int zero = 0;
+  if (cudaMemcpy(static_cast<char*>(workspace) + offsetof(WsHeader, error), &zero, sizeof(int),
+                 cudaMemcpyHostToDevice) != cudaSuccess)
+    return SV_ECUDA;
+  if (device_flags) *device_flags = h.error;
+  if (h.error & SV_DERR_TIMEOUT) return SV_ETIMEOUT;
+  return h.error ? SV_EDATA : SV_OK;
+}
+
+sv_status sv_selftest_wait_timeout(void* workspace, size_t ws_bytes, int64_t limit_ns,
+                                   sv_stream_t stream) {
+  if (workspace == nullptr || ws_bytes < sizeof(WsHeader) ||
+      (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0)
+    return SV_EWORKSPACE;
+  if (limit_ns <= 0 || limit_ns > 2000000000ll) return SV_EINVAL;
+  DeviceInfo dev;
+  const sv_status ds = device_info(dev);
+  if (ds != SV_OK) return ds;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  wait_selftest_kernel<<<1, 32, 0, s>>>(static_cast<WsHeader*>(workspace),
+                                        static_cast<uint64_t>(limit_ns));
+  if (cudaGetLastError() != cudaSuccess) return SV_ECUDA;
+  return sv_get_error(workspace, stream, nullptr);
+}
+
+}  // extern "C"

@@ -1,0 +1,416 @@
+// sv_rowpass.cuh -- the streaming row pass shared by the chain and tree
+// kernels, and the inverse-CDF draw.
+//
+// One persistent CTA per SM: warp 8 is the producer, warps 0..7 consume.
+// Work is a flat list of "items"; an item is one 32 KB chunk of one logit
+// row that the step must read (target rows 0..nd and, for sampled requests,
+// draft rows 0..nd-1).  The producer claims items with a global atomic
+// counter and moves each one into a 4-stage shared-memory ring with a 1-D
+// bulk copy (the TMA engine), completion tracked by an mbarrier.  Consumers
+// reduce the chunk to a partial -- (max, sum exp) for sampled rows, (max,
+// lowest argmax) for greedy rows -- and write it to the workspace.  A
+// per-request ticket counts finished items; the CTA that finishes the last
+// item of a request runs that request's finalize (acceptance scan, residual
+// draw) while its producer keeps streaming.  No CTA ever waits for another.
+#pragma once
+
+#include "sv_device.cuh"
+
+namespace sv {
+
+constexpr int kStages = 4;
+constexpr int kChunkBytes = 32768;
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;
+constexpr int kSegEl = 1024;        // inverse-CDF segment: 32 lanes x 32 elements
+constexpr int kMaxSeg = 1024;       // => V <= 2^20
+constexpr int kMaxRowsPerReq = 128;  // chain: 2K+1 <= 65; tree: N + M <= 128
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+constexpr uint64_t kWaitLimitAfterTimeoutNs = 1000000ull;  // 1 ms
+
+enum RowKind : int { KIND_ARGMAX = 0, KIND_SOFTMAX = 1, KIND_TOPK = 2 };
+
+struct WsHeader {
+  unsigned int work_counter;
+  unsigned int done_ctas;
+  int error;
+  int pad;
+};
+
+// Device view of the caller's workspace.
+struct Ws {
+  WsHeader* hdr;
+  unsigned int* tickets;  // [B]
+  float2* partials;       // [rows_max * ipr]
+  float* scratch;         // per-request residual rows (tree walk) [B][V]
+};
+
+struct StageMeta {
+  int item;      // -1: no more work
+  int pos;       // request position in processing order
+  int row;       // flat row id (processing order)
+  int kind;
+  int n_el;      // elements in this chunk
+  int el_base;   // first element's index within the row
+  float c_hi, c_lo;
+  const char* src;
+};
+
+struct FinScratch {
+  double dsum[kConsumerWarps];
+  float seg[kMaxSeg];
+  float rm[kMaxRowsPerReq];
+  float rz[kMaxRowsPerReq];
+  int ridx[kMaxRowsPerReq];
+  double base;
+  int seg_k;
+  int seg_mode;  // 0 normal, 1 take the last positive weight, 2 no mass
+  int n_acc;
+  int err;
+  int token;
+  int misc[8];
+};
+
+struct Shared {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  StageMeta meta[kStages];
+  MS red_ms[2][kConsumerWarps];
+  VI red_vi[2][kConsumerWarps];
+  int fin_pending;
+  int n_pos;
+  int timed_out;  // a bounded wait of this CTA expired: later waits are short
+  int pad;
+  FinScratch fin;
+};
+
+// Per-position tables that follow Shared in dynamic shared memory.
+struct PosTables {
+  int* info;      // request id | kind << 16 | extra << 20
+  int* rstart;    // [n_pos + 1] first flat row of each position
+  float2* scale;  // log2(e)/t pair per position
+  unsigned long long* aux;  // tree: referenced draft rows per position
+};
+
+__device__ __forceinline__ int info_req(int info) { return info & 0xffff; }
+__device__ __forceinline__ int info_kind(int info) { return (info >> 16) & 3; }
+__device__ __forceinline__ int info_extra(int info) { return (info >> 20) & 0x7ff; }
+__device__ __forceinline__ int make_info(int b, int kind, int extra) {
+  return b | (kind << 16) | (extra << 20);
+}
+
+// log2(e)/t as a float pair computed with fp32 divisions only: hi is the
+// quotient rounded down, lo the quotient of the exact (non-negative)
+// remainder.  Both parts are positive, so a -inf logit scales to -inf in
+// both products and never meets +inf.
+__device__ __forceinline__ Scale2 scale_for(float t) {
+  const float l_hi = 1.44269502162933349609375f;     // fl(log2 e)
+  const float l_lo = 1.925963033500011079e-08f;      // log2 e - l_hi
+  Scale2 c;
+  if (!(t > 0.f)) {
+    c.hi = 0.f;
+    c.lo = 0.f;
+    return c;
+  }
+  c.hi = __fdiv_rd(l_hi, t);
+  const float rem = fmaf(-c.hi, t, l_hi);
+  c.lo = fmaxf(__fdiv_rn(rem + l_lo, t), 1.0e-45f);
+  return c;
+}
+
+// Block-wide (all kThreads) exclusive scan of int4 values.
+__device__ __forceinline__ int4 block_excl_scan4(int4 v, int4* warp_tot, int4& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int4 inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int4 y;
+    y.x = __shfl_up_sync(0xffffffffu, inc.x, o);
+    y.y = __shfl_up_sync(0xffffffffu, inc.y, o);
+    y.z = __shfl_up_sync(0xffffffffu, inc.z, o);
+    y.w = __shfl_up_sync(0xffffffffu, inc.w, o);
+    if (lane >= o) {
+      inc.x += y.x;
+      inc.y += y.y;
+      inc.z += y.z;
+      inc.w += y.w;
+    }
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  int4 before = make_int4(0, 0, 0, 0);
+  total = make_int4(0, 0, 0, 0);
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const int4 t = warp_tot[w];
+    if (w < warp) {
+      before.x += t.x;
+      before.y += t.y;
+      before.z += t.z;
+      before.w += t.w;
+    }
+    total.x += t.x;
+    total.y += t.y;
+    total.z += t.z;
+    total.w += t.w;
+  }
+  __syncthreads();
+  return make_int4(before.x + inc.x - v.x, before.y + inc.y - v.y, before.z + inc.z - v.z,
+                   before.w + inc.w - v.w);
+}
+
+// ------------------------------------------------------------ chunk reduce
+
+// Fast path: bf16 chunk staged in shared memory.  Each consumer thread
+// takes up to eight 16-byte vectors, releases the stage as soon as they are
+// in registers, then reduces.
+template <int KIND>
+__device__ __forceinline__ void reduce_chunk_bf16(const StageMeta& mt, const uint4* stage,
+                                                  uint64_t* empty_bar, int ctid, int lane,
+                                                  MS& ms, VI& vi) {
+  const int nvec = mt.n_el >> 3;
+  uint4 r[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int v = ctid + k * kConsumers;
+    r[k] = v < nvec ? stage[v] : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(empty_bar);
+
+  uint32_t mx2 = 0xff80ff80u;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    mx2 = bf16x2_max_nan(mx2, r[k].x);
+    mx2 = bf16x2_max_nan(mx2, r[k].y);
+    mx2 = bf16x2_max_nan(mx2, r[k].z);
+    mx2 = bf16x2_max_nan(mx2, r[k].w);
+  }
+  const float a = bf16lo(mx2), b = bf16hi(mx2);
+  float m = (a != a || b != b) ? __int_as_float(0x7fc00000) : fmaxf(a, b);
+  if (m == kPosInf) m = __int_as_float(0x7fc00000);
+
+  if (KIND == KIND_SOFTMAX) {
+    float s = 0.f;
+    if (m == m && m != kNegInf) {
+      const Scale2 c{mt.c_hi, mt.c_lo};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t w[4] = {r[k].x, r[k].y, r[k].z, r[k].w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          s += fast_exp2(scaled_arg(bf16lo(w[h]), m, c));
+          s += fast_exp2(scaled_arg(bf16hi(w[h]), m, c));
+        }
+      }
+    }
+    ms = MS{m, s};
+  } else {
+    int idx = 0x7fffffff;
+    if (m == m) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int v = ctid + k * kConsumers;
+        const uint32_t w[4] = {r[k].x, r[k].y, r[k].z, r[k].w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const int e = mt.el_base + v * 8 + 2 * h;
+          if (v < nvec && idx == 0x7fffffff) {
+            if (bf16lo(w[h]) == m) idx = e;
+            else if (bf16hi(w[h]) == m) idx = e + 1;
+          }
+        }
+      }
+    }
+    vi = VI{m, idx};
+  }
+}
+
+// Generic path: any dtype, chunk either staged (bulk) or read from global.
+template <int KIND>
+__device__ __forceinline__ void reduce_chunk_generic(const StageMeta& mt, const char* stage,
+                                                     bool staged, int es,
+                                                     uint64_t* empty_bar, int ctid, int lane,
+                                                     MS& ms, VI& vi) {
+  const char* base = staged ? stage : mt.src;
+  auto ld = [&](int e) -> float {
+    if (es == 2) return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(base)[e]);
+    return reinterpret_cast<const float*>(base)[e];
+  };
+  // ascending index within the thread: strict ">" keeps the lowest index
+  float m = kNegInf;
+  bool bad = false;
+  int idx = 0x7fffffff;
+  for (int e = ctid; e < mt.n_el; e += kConsumers) {
+    const float x = ld(e);
+    if (x != x || x == kPosInf) bad = true;
+    if (idx == 0x7fffffff || x > m) {
+      m = x;
+      idx = mt.el_base + e;
+    }
+  }
+  if (KIND == KIND_SOFTMAX) {
+    float s = 0.f;
+    if (!bad && m != kNegInf) {
+      const Scale2 c{mt.c_hi, mt.c_lo};
+      for (int e = ctid; e < mt.n_el; e += kConsumers) s += fast_exp2(scaled_arg(ld(e), m, c));
+    }
+    ms = bad ? MS{__int_as_float(0x7fc00000), 0.f} : MS{m, s};
+  } else {
+    vi = bad ? VI{__int_as_float(0x7fc00000), 0} : VI{m, idx};
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(empty_bar);
+}
+
+// ---------------------------------------------------------- inverse CDF
+
+// Draw by inverse CDF from 32-element weight blocks produced by wf(i0, w)
+// (w[j] = weight of token i0 + j, zero beyond V): the smallest t with
+// u * S < C(t), C the running sum over ascending id, S the total; if
+// rounding leaves none, the largest t with positive weight.  Sums: fp32
+// within a lane (sequential) and across lanes (warp scan); fp64 across
+// segments and for the final comparisons.  Called by all kConsumers
+// threads; returns the token (-1 if S == 0) in every thread.
+template <class WF>
+__device__ int icdf_draw(int V, double u, const WF& wf, FinScratch& fs, int ctid) {
+  const int warp = ctid >> 5, lane = ctid & 31;
+  const int nseg = (V + kSegEl - 1) / kSegEl;
+  for (int s = warp; s < nseg; s += kConsumerWarps) {
+    float w[32];
+    wf(s * kSegEl + lane * 32, w);
+    float ls = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) ls += w[j];
+    const float inc = warp_incl_scan(ls, lane);
+    if (lane == 31) fs.seg[s] = inc;
+  }
+  named_sync(1, kConsumers);
+  if (warp == 0) {
+    const int per = (nseg + 31) / 32;
+    const int lo = min(lane * per, nseg), hi = min(lo + per, nseg);
+    double lt = 0.0;
+    for (int s = lo; s < hi; ++s) lt += static_cast<double>(fs.seg[s]);
+    const double incl = warp_incl_scan_d(lt, lane);
+    double excl = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) excl = 0.0;
+    const double S = __shfl_sync(0xffffffffu, incl, 31);
+    const double target = u * S;
+    int found = -1;
+    double base = 0.0, run = excl;
+    int last_pos = -1;
+    for (int s = lo; s < hi; ++s) {
+      const double nxt = run + static_cast<double>(fs.seg[s]);
+      if (found < 0 && target < nxt) {
+        found = s;
+        base = run;
+      }
+      if (fs.seg[s] > 0.f) last_pos = s;
+      run = nxt;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, found >= 0);
+    const unsigned pos = __ballot_sync(0xffffffffu, last_pos >= 0);
+    if (lane == 0) {
+      fs.seg_mode = 2;
+      fs.seg_k = -1;
+    }
+    __syncwarp();
+    if (!(S > 0.0)) {
+      // no mass: mode 2
+    } else if (hit) {
+      const int src = __ffs(hit) - 1;
+      if (lane == src) {
+        fs.seg_k = found;
+        fs.base = base;
+        fs.seg_mode = 0;
+      }
+    } else if (pos) {
+      const int src = 31 - __clz(pos);
+      if (lane == src) {
+        fs.seg_k = last_pos;
+        fs.seg_mode = 1;
+      }
+    }
+    __syncwarp();
+    if (fs.seg_mode != 2) {
+      const int k = fs.seg_k;
+      float w[32];
+      wf(k * kSegEl + lane * 32, w);
+      float ls = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) ls += w[j];
+      const float inc = warp_incl_scan(ls, lane);
+      float exl = __shfl_up_sync(0xffffffffu, inc, 1);
+      if (lane == 0) exl = 0.f;
+      int tok = -1;
+      if (fs.seg_mode == 0) {
+        const bool lane_hit = target < fs.base + static_cast<double>(inc);
+        const unsigned lh = __ballot_sync(0xffffffffu, lane_hit);
+        const int src = lh ? __ffs(lh) - 1 : 31;
+        if (lane == src) {
+          double c = fs.base + static_cast<double>(exl);
+          int lastp = -1;
+          for (int j = 0; j < 32; ++j) {
+            c += static_cast<double>(w[j]);
+            if (w[j] > 0.f) lastp = j;
+            if (tok < 0 && target < c) tok = j;
+          }
+          if (tok < 0) tok = lastp;
+          tok = tok < 0 ? -1 : k * kSegEl + lane * 32 + tok;
+        }
+        tok = __shfl_sync(0xffffffffu, tok, src);
+      } else {
+        int lastp = -1;
+        for (int j = 0; j < 32; ++j)
+          if (w[j] > 0.f) lastp = j;
+        const unsigned lp = __ballot_sync(0xffffffffu, lastp >= 0);
+        const int src = lp ? 31 - __clz(lp) : 0;
+        tok = __shfl_sync(0xffffffffu, lastp < 0 ? -1 : k * kSegEl + lane * 32 + lastp, src);
+      }
+      if (lane == 0) fs.token = tok;
+    } else if (lane == 0) {
+      fs.token = -1;
+    }
+  }
+  named_sync(1, kConsumers);
+  const int tok = fs.token;
+  named_sync(1, kConsumers);
+  return tok;
+}
+
+// Load 32 consecutive logits [i0, i0+32) of a row as floats (0 beyond V is
+// NOT applied here; `valid` counts the in-range ones).
+__device__ __forceinline__ void load32(const char* row, int es, bool vec_ok, int i0, int V,
+                                       float* x) {
+  if (es == 2 && vec_ok && i0 + 32 <= V) {
+    const uint4* p = reinterpret_cast<const uint4*>(row + static_cast<size_t>(i0) * 2);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 v = __ldg(p + q);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        x[q * 8 + 2 * h] = bf16lo(w[h]);
+        x[q * 8 + 2 * h + 1] = bf16hi(w[h]);
+      }
+    }
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int t = i0 + j;
+    if (t < V) {
+      x[j] = es == 2 ? bf16_bits_to_float(__ldg(reinterpret_cast<const uint16_t*>(row) + t))
+                     : __ldg(reinterpret_cast<const float*>(row) + t);
+    } else {
+      x[j] = kNegInf;
+    }
+  }
+}
+
+__device__ __forceinline__ float load_logit(const char* row, int es, int t) {
+  return es == 2 ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(row)[t])
+                 : reinterpret_cast<const float*>(row)[t];
+}
+
+}  // namespace sv
