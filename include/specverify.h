@@ -77,7 +77,7 @@ typedef enum {
 
 /* Limits of this implementation. */
 #define SV_MAX_K 32        /* drafts per chain */
-#define SV_MAX_B 4096      /* requests per call */
+#define SV_MAX_B 1024      /* requests per call */
 #define SV_MAX_V (1 << 20) /* vocabulary entries */
 #define SV_MAX_TOPK 256    /* top-k filter size */
 #define SV_MAX_TREE_NODES 64 /* nodes per tree (N) and draft rows (M) */

@@ -2,10 +2,12 @@
 // argument checks, workspace layout, launch of the sm_103a kernels.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "specverify.h"
 #include "sv_chain.cuh"
+#include "sv_resid.cuh"
 #include "sv_tree.cuh"
 
 namespace {
@@ -16,7 +18,7 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 struct Layout {
-  size_t tickets, partials, scratch, total;
+  size_t tickets, jobs, partials, scratch, total;
 };
 
 // The header and the per-request tickets sit at fixed offsets with a fixed
@@ -26,7 +28,8 @@ struct Layout {
 Layout layout_for(int64_t /*B*/, int64_t rows_max, int64_t ipr, int64_t scratch_floats) {
   Layout L;
   L.tickets = align_up(sizeof(WsHeader));
-  L.partials = align_up(L.tickets + sizeof(unsigned int) * static_cast<size_t>(SV_MAX_B));
+  L.jobs = align_up(L.tickets + sizeof(unsigned int) * static_cast<size_t>(SV_MAX_B));
+  L.partials = align_up(L.jobs + sizeof(ResidJob) * static_cast<size_t>(SV_MAX_B));
   L.scratch = align_up(L.partials + sizeof(float2) * static_cast<size_t>(rows_max * ipr));
   L.total = align_up(L.scratch + sizeof(float) * static_cast<size_t>(scratch_floats));
   return L;
@@ -38,12 +41,23 @@ Ws ws_view(void* base, const Layout& L) {
   w.hdr = reinterpret_cast<WsHeader*>(p);
   w.tickets = reinterpret_cast<unsigned int*>(p + L.tickets);
   w.partials = reinterpret_cast<float2*>(p + L.partials);
+  w.jobs = reinterpret_cast<void*>(p + L.jobs);
   w.scratch = reinterpret_cast<float*>(p + L.scratch);
   return w;
 }
 
 int es_of(sv_dtype d) { return d == SV_BF16 ? 2 : 4; }
 int chunk_el_of(sv_dtype d) { return kChunkBytes / es_of(d); }
+int resid_chunk_el_of(sv_dtype d) { return kChunkBytes / 2 / es_of(d); }
+
+// Chain calls: the chain pass stores per-row chunk partials, the residual
+// pass per-job segment sums, in the same region (the passes run in turn).
+Layout chain_layout(int64_t B, int64_t K, int64_t V, sv_dtype dtype) {
+  const int64_t ipr = (V + chunk_el_of(dtype) - 1) / chunk_el_of(dtype);
+  const int64_t ipr2 = (V + resid_chunk_el_of(dtype) - 1) / resid_chunk_el_of(dtype);
+  const int64_t slots = std::max(B * (2 * K + 1) * ipr, B * ipr2 * kConsumerWarps);
+  return layout_for(B, slots, 1, 0);
+}
 
 // Per-device facts, looked up once.
 struct DeviceInfo {
@@ -73,15 +87,14 @@ sv_status device_info(DeviceInfo& out) {
   return out.supported ? SV_OK : SV_EUNSUPPORTED;
 }
 
-size_t pos_table_bytes(int n_req, bool aux) {
-  return (sizeof(float2) + (aux ? 8 : 0)) * n_req + sizeof(int) * n_req +
-         sizeof(int) * (n_req + 1);
+size_t pos_table_bytes(int n_req, int aux_bytes) {
+  return (sizeof(float2) + aux_bytes) * n_req + sizeof(int) * n_req + sizeof(int) * (n_req + 1);
 }
 
 template <class P>
 size_t kernel_smem(int n_req) {
-  return static_cast<size_t>(kStages) * kChunkBytes + ((sizeof(Shared) + 15) & ~size_t(15)) +
-         pos_table_bytes(n_req, P::kAux);
+  return 128 + static_cast<size_t>(kStages) * kChunkBytes +
+         ((sizeof(Shared) + 15) & ~size_t(15)) + pos_table_bytes(n_req, P::kAuxBytes);
 }
 
 template <class P>
@@ -139,8 +152,7 @@ size_t sv_chain_workspace_bytes(int32_t B, int32_t K, int32_t V, sv_dtype dtype,
   if (B < 0 || B > SV_MAX_B || K < 0 || K > SV_MAX_K || V < 1 || V > SV_MAX_V ||
       (dtype != SV_BF16 && dtype != SV_FP32) || max_top_k < 0 || max_top_k > SV_MAX_TOPK)
     return 0;
-  const int64_t ipr = (V + chunk_el_of(dtype) - 1) / chunk_el_of(dtype);
-  return layout_for(B, static_cast<int64_t>(B) * (2 * K + 1), ipr, 0).total;
+  return chain_layout(B, K, V, dtype).total;
 }
 
 size_t sv_tree_workspace_bytes(int32_t B, int32_t N, int32_t M, int32_t V, sv_dtype dtype,
@@ -187,7 +199,7 @@ sv_status sv_verify_chain(const sv_chain_args* a, void* workspace, size_t ws_byt
   const int es = es_of(a->dtype);
   const int chunk_el = chunk_el_of(a->dtype);
   const int ipr = (a->V + chunk_el - 1) / chunk_el;
-  const Layout L = layout_for(a->B, static_cast<int64_t>(a->B) * (2 * a->K + 1), ipr, 0);
+  const Layout L = chain_layout(a->B, a->K, a->V, a->dtype);
 
   ChainProblem p;
   p.n_req = a->B;
@@ -215,10 +227,36 @@ sv_status sv_verify_chain(const sv_chain_args* a, void* workspace, size_t ws_byt
   p.p_at = a->p_at_draft;
   p.q_at = a->q_at_draft;
   p.ws = ws_view(workspace, L);
+  p.jobs = static_cast<ResidJob*>(p.ws.jobs);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
   const int64_t items_max = static_cast<int64_t>(a->B) * (2 * a->K + 1) * ipr;
-  const int grid = static_cast<int>(items_max < dev.sms ? (items_max < 1 ? 1 : items_max) : dev.sms);
-  return launch(p, grid, reinterpret_cast<cudaStream_t>(stream));
+  const int grid = static_cast<int>(std::min<int64_t>(std::max<int64_t>(items_max, 1), dev.sms));
+  sv_status st = launch(p, grid, s);
+  if (st != SV_OK) return st;
+
+  // residual / bonus draws of the sampled requests, over the whole GPU
+  ResidProblem r;
+  r.n_req = a->B;
+  r.K = a->K;
+  r.V = a->V;
+  r.es = es;
+  r.chunk_el = resid_chunk_el_of(a->dtype);
+  r.ipr = (a->V + r.chunk_el - 1) / r.chunk_el;
+  r.bulk = p.bulk;
+  r.target = p.target;
+  r.t_stride = p.t_stride;
+  r.draft = p.draft;
+  r.d_stride = p.d_stride;
+  r.uniforms = a->uniforms;
+  r.out_tokens = a->out_tokens;
+  r.out_len = a->out_len;
+  r.accept_len = a->accept_len;
+  r.jobs = p.jobs;
+  r.ws = p.ws;
+  const int64_t items2 = static_cast<int64_t>(a->B) * r.ipr;
+  const int grid2 = static_cast<int>(std::min<int64_t>(std::max<int64_t>(items2, 1), dev.sms));
+  return launch(r, grid2, s);
 }
 
 sv_status sv_verify_tree(const sv_tree_args* a, void* workspace, size_t ws_bytes,
@@ -281,7 +319,7 @@ sv_status sv_verify_tree(const sv_tree_args* a, void* workspace, size_t ws_bytes
   p.ws = ws_view(workspace, L);
 
   const int64_t items_max = static_cast<int64_t>(a->B) * (a->N + a->M) * ipr;
-  const int grid = static_cast<int>(items_max < dev.sms ? (items_max < 1 ? 1 : items_max) : dev.sms);
+  const int grid = static_cast<int>(std::min<int64_t>(std::max<int64_t>(items_max, 1), dev.sms));
   return launch(p, grid, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -9,12 +9,12 @@
 // argmax of target row i (lecture notes sec. 2.2; study notes sec. 10).
 #pragma once
 
-#include "sv_kernel.cuh"
+#include "sv_resid.cuh"
 
 namespace sv {
 
 struct ChainProblem {
-  static constexpr bool kAux = false;
+  static constexpr int kAuxBytes = 0;
   int n_req, K, V, es, ipr, chunk_el, max_topk;
   bool bulk;
   const char* target;
@@ -31,6 +31,7 @@ struct ChainProblem {
   int* accept_len;
   float* p_at;
   float* q_at;
+  ResidJob* jobs;  // sampled requests leave their residual / bonus draw here
   Ws ws;
 
   // kind of request b, or -1 if its scalar arguments are invalid
@@ -109,22 +110,28 @@ struct ChainProblem {
     }
   }
 
-  __device__ const char* row_ptr(const PosTables& tab, int pos, int rl, int& kind,
-                                 Scale2& c) const {
-    const int info = tab.info[pos];
+  __device__ void fill_stage(const PosTables& tab, int rl, StageMeta& mt) const {
+    const int info = tab.info[mt.pos];
     const int b = info_req(info), nd = info_extra(info);
-    kind = info_kind(info);
-    const float2 s = tab.scale[pos];
-    c.hi = s.x;
-    c.lo = s.y;
-    if (rl <= nd) return target + (static_cast<int64_t>(b) * (K + 1) + rl) * t_stride;
-    return draft + (static_cast<int64_t>(b) * K + (rl - nd - 1)) * d_stride;
+    mt.kind = info_kind(info);
+    const float2 s = tab.scale[mt.pos];
+    mt.c_hi = s.x;
+    mt.c_lo = s.y;
+    const char* rp = rl <= nd ? target + (static_cast<int64_t>(b) * (K + 1) + rl) * t_stride
+                              : draft + (static_cast<int64_t>(b) * K + (rl - nd - 1)) * d_stride;
+    mt.src = rp + static_cast<size_t>(mt.el_base) * es;
   }
 
-  __device__ void finalize(Shared& sh, const PosTables& tab, int pos, int ctid) const;
+  __device__ float2 consume(const StageMeta& mt, const unsigned char* sp, uint64_t* empty_bar,
+                            int ctid, int lane) const {
+    return reduce_row_chunk(mt, sp, empty_bar, ctid, lane, bulk, es);
+  }
+
+  __device__ void finalize(Shared& sh, const PosTables& tab, int pos, int ftid) const;
+  __device__ void last_cta_reset() const {}
 };
 
-// Residual / bonus weights of 32 consecutive tokens.
+// Residual / bonus weights of 32 consecutive tokens (tree walk helper).
 struct ChainWeights {
   const char* prow;
   const char* qrow;  // nullptr: bonus mode, w = 2^((l - m_p) c)
@@ -152,9 +159,9 @@ struct ChainWeights {
 };
 
 __device__ void ChainProblem::finalize(Shared& sh, const PosTables& tab, int pos,
-                                       int ctid) const {
+                                       int ftid) const {
   FinScratch& fs = sh.fin;
-  const int warp = ctid >> 5, lane = ctid & 31;
+  const int warp = ftid >> 5, lane = ftid & 31;
   const int info = tab.info[pos];
   const int b = info_req(info), kind = info_kind(info), nd = info_extra(info);
   const int r0 = tab.rstart[pos];
@@ -162,34 +169,51 @@ __device__ void ChainProblem::finalize(Shared& sh, const PosTables& tab, int pos
   const Scale2 c{tab.scale[pos].x, tab.scale[pos].y};
   const bool greedy = kind == KIND_ARGMAX;
 
-  // (1) merge the chunk partials of every row of this request
-  for (int j = warp; j < nrows; j += kConsumerWarps) {
-    const float2* pp = ws.partials + static_cast<size_t>(r0 + j) * ipr;
-    if (greedy) {
-      VI v{kNegInf, 0x7fffffff};
-      for (int ch = lane; ch < ipr; ch += 32) {
-        const float2 t = __ldcg(pp + ch);
-        v = vi_better(v, VI{t.x, __float_as_int(t.y)});
-      }
-      v = warp_reduce_vi(v);
-      if (lane == 0) {
-        fs.rm[j] = v.v;
-        fs.ridx[j] = v.i;
-      }
-    } else {
-      MS v{kNegInf, 0.f};
-      for (int ch = lane; ch < ipr; ch += 32) {
-        const float2 t = __ldcg(pp + ch);
-        v = ms_combine(v, MS{t.x, t.y}, c);
-      }
-      v = warp_reduce_ms(v, c);
-      if (lane == 0) {
-        fs.rm[j] = v.m;
-        fs.rz[j] = v.s;
+  // (1) merge the chunk partials of every row: a warp takes 32 / ipr rows
+  // per pass, one group of ipr lanes per row (all loads issued first), then
+  // a guarded shfl_down tree within each group
+  {
+    const int width = ipr <= 32 ? ipr : 32;
+    const int rpw = 32 / width;
+    const int g = lane / width, r = lane % width;
+    for (int j0 = warp * rpw; j0 < nrows; j0 += kFinWarps * rpw) {
+      const int j = j0 + g;
+      const bool own = g < rpw && j < nrows;
+      const float2* pp = ws.partials + static_cast<size_t>(r0 + (own ? j : 0)) * ipr;
+      if (greedy) {
+        VI v{kNegInf, 0x7fffffff};
+        if (own)
+          for (int ch = r; ch < ipr; ch += width) {
+            const float2 u = __ldcg(pp + ch);
+            v = vi_better(v, VI{u.x, __float_as_int(u.y)});
+          }
+        for (int o = 1; o < width; o <<= 1) {
+          const VI w{__shfl_down_sync(0xffffffffu, v.v, o), __shfl_down_sync(0xffffffffu, v.i, o)};
+          if (r + o < width) v = vi_better(v, w);
+        }
+        if (own && r == 0) {
+          fs.rm[j] = v.v;
+          fs.ridx[j] = v.i;
+        }
+      } else {
+        MS v{kNegInf, 0.f};
+        if (own)
+          for (int ch = r; ch < ipr; ch += width) {
+            const float2 u = __ldcg(pp + ch);
+            v = ms_combine(v, MS{u.x, u.y}, c);
+          }
+        for (int o = 1; o < width; o <<= 1) {
+          const MS w{__shfl_down_sync(0xffffffffu, v.m, o), __shfl_down_sync(0xffffffffu, v.s, o)};
+          if (r + o < width) v = ms_combine(v, w, c);
+        }
+        if (own && r == 0) {
+          fs.rm[j] = v.m;
+          fs.rz[j] = v.s;
+        }
       }
     }
   }
-  named_sync(1, kConsumers);
+  named_sync(1, kFinThreads);
 
   // (2) accept tests and the prefix-terminating scan (warp 0, lane i = draft i)
   if (warp == 0) {
@@ -240,61 +264,46 @@ __device__ void ChainProblem::finalize(Shared& sh, const PosTables& tab, int pos
       fs.err = err;
     }
   }
-  named_sync(1, kConsumers);
+  named_sync(1, kFinThreads);
   const int n = fs.n_acc;
   const int err = fs.err;
 
-  // (3) the emitted token
+  // (3) the emitted token: greedy here; sampled requests hand the draw to
+  // the residual pass (one job: row pair n, residual or bonus)
   int token = -1;
-  int err2 = err;
-  if (!err) {
-    if (greedy) {
-      token = fs.ridx[n];
-    } else {
-      const double u = static_cast<double>(uniforms[static_cast<size_t>(b) * (K + 1) + K]);
-      ChainWeights wf;
-      wf.prow = target + (static_cast<int64_t>(b) * (K + 1) + n) * t_stride;
-      wf.mp = fs.rm[n];
-      wf.izp = 1.f / fs.rz[n];
-      wf.c = c;
-      wf.es = es;
-      wf.V = V;
-      wf.vec_ok = bulk;
-      if (n < nd) {
-        wf.qrow = draft + (static_cast<int64_t>(b) * K + n) * d_stride;
-        wf.mq = fs.rm[nd + 1 + n];
-        wf.izq = 1.f / fs.rz[nd + 1 + n];
-      } else {
-        wf.qrow = nullptr;
-        wf.mq = 0.f;
-        wf.izq = 0.f;
-      }
-      token = icdf_draw(V, u, wf, fs, ctid);
-      if (token < 0 && wf.qrow != nullptr) {
-        // residual of zero mass (rounding only): draw from p_n instead
-        wf.qrow = nullptr;
-        token = icdf_draw(V, u, wf, fs, ctid);
-      }
-      if (token < 0) err2 |= 0x04;
-    }
+  const int err2 = err;
+  if (!err && greedy) token = fs.ridx[n];
+  if (!err && !greedy && ftid == 0) {
+    const int jid = atomicAdd(&ws.hdr->n_jobs, 1);
+    ResidJob jb;
+    jb.b = b;
+    jb.n = n;
+    jb.mode = n < nd ? 0 : 1;
+    jb.mp = fs.rm[n];
+    jb.izp = 1.f / fs.rz[n];
+    jb.mq = n < nd ? fs.rm[nd + 1 + n] : 0.f;
+    jb.izq = n < nd ? 1.f / fs.rz[nd + 1 + n] : 0.f;
+    jb.c_hi = c.hi;
+    jb.c_lo = c.lo;
+    jobs[jid] = jb;
   }
 
   // (4) outputs; reset this request's ticket for the next call
-  if (ctid <= K) {
+  if (ftid <= K) {
     int v = -1;
     if (!err2) {
-      if (ctid < n) v = tokens[static_cast<size_t>(b) * K + ctid];
-      else if (ctid == n) v = token;
+      if (ftid < n) v = tokens[static_cast<size_t>(b) * K + ftid];
+      else if (ftid == n) v = token;  // sampled: written by the residual pass
     }
-    out_tokens[static_cast<size_t>(b) * (K + 1) + ctid] = v;
+    out_tokens[static_cast<size_t>(b) * (K + 1) + ftid] = v;
   }
-  if (ctid == 0) {
+  if (ftid == 0) {
     out_len[b] = err2 ? 0 : n + 1;
     accept_len[b] = err2 ? 0 : n;
     if (err2) record_error(&ws.hdr->error, err2);
     ws.tickets[b] = 0u;
   }
-  named_sync(1, kConsumers);
+  named_sync(1, kFinThreads);
 }
 
 }  // namespace sv

@@ -61,6 +61,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test: has the phase with the given parity completed?
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait until the phase with the given parity has completed, for at most
 // limit_ns nanoseconds.  Returns false when the limit expired.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
@@ -145,15 +158,19 @@ __device__ __forceinline__ MS ms_combine(MS a, MS b, Scale2 c) {
   return MS{m, s};
 }
 
+// Warp-wide combination of (m, s) pairs: the maximum first, then each lane
+// rescales its sum once to the common maximum and the sums are added.
 __device__ __forceinline__ MS warp_reduce_ms(MS v, Scale2 c) {
+  const bool bad = __any_sync(0xffffffffu, v.m != v.m);
+  float m = v.m;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    MS w;
-    w.m = __shfl_xor_sync(0xffffffffu, v.m, o);
-    w.s = __shfl_xor_sync(0xffffffffu, v.s, o);
-    v = ms_combine(v, w, c);
-  }
-  return v;
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (bad) return MS{__int_as_float(0x7fc00000), 0.f};
+  if (m == kNegInf) return MS{kNegInf, 0.f};
+  float s = v.m == kNegInf ? 0.f : v.s * fast_exp2(scaled_arg(v.m, m, c));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return MS{m, s};
 }
 
 // Argmax pair: value and lowest index attaining it.  NaN value marks a row
@@ -200,5 +217,16 @@ __device__ __forceinline__ double warp_incl_scan_d(double x, int lane) {
 }
 
 __device__ __forceinline__ void record_error(int* err, int flag) { atomicOr(err, flag); }
+
+// Fetch-and-add with acquire-release semantics at GPU scope: orders this
+// thread's earlier stores before the add (release) and, for the thread that
+// reads the final count, makes every earlier releaser's stores visible
+// (acquire).  No separate fence is needed on the hot path.
+__device__ __forceinline__ unsigned atomic_add_acq_rel(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
 
 }  // namespace sv

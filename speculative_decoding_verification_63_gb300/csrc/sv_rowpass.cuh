@@ -1,17 +1,18 @@
-// sv_rowpass.cuh -- the streaming row pass shared by the chain and tree
-// kernels, and the inverse-CDF draw.
+// sv_rowpass.cuh -- definitions shared by the verification kernels: the
+// CTA layout, shared-memory state, workspace view, chunk reductions and the
+// inverse-CDF draw.
 //
-// One persistent CTA per SM: warp 8 is the producer, warps 0..7 consume.
 // Work is a flat list of "items"; an item is one 32 KB chunk of one logit
 // row that the step must read (target rows 0..nd and, for sampled requests,
-// draft rows 0..nd-1).  The producer claims items with a global atomic
-// counter and moves each one into a 4-stage shared-memory ring with a 1-D
-// bulk copy (the TMA engine), completion tracked by an mbarrier.  Consumers
-// reduce the chunk to a partial -- (max, sum exp) for sampled rows, (max,
-// lowest argmax) for greedy rows -- and write it to the workspace.  A
-// per-request ticket counts finished items; the CTA that finishes the last
-// item of a request runs that request's finalize (acceptance scan, residual
-// draw) while its producer keeps streaming.  No CTA ever waits for another.
+// draft rows 0..nd-1).  A producer warp claims items and moves each into a
+// 4-stage shared-memory ring with a 1-D bulk copy (the TMA engine);
+// consumer warps reduce the chunk -- (max, sum of exp) for sampled rows,
+// (max, lowest argmax) for greedy rows -- and hand per-warp partials to a
+// bookkeeper warp through a result ring; the bookkeeper combines them,
+// stores one partial per chunk and counts per-request tickets; a finalizer
+// group runs the finalize of each request whose last chunk is in (accept
+// scan, emitted token) while the consumers keep streaming.  Every hand-off
+// inside a CTA is an mbarrier; no CTA ever waits for another.
 #pragma once
 
 #include "sv_device.cuh"
@@ -20,30 +21,41 @@ namespace sv {
 
 constexpr int kStages = 4;
 constexpr int kChunkBytes = 32768;
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;
+constexpr int kVecPerThread = kChunkBytes / 16 / kConsumers;  // 16-byte vectors per chunk
+constexpr int kResSlots = 16;                 // result ring (consumers -> bookkeeper)
+constexpr int kFinWarps = 4;                  // finalizer group
+constexpr int kFinThreads = kFinWarps * 32;
+constexpr int kProducerThread = kConsumers;   // lane 0 of the producer warp
+constexpr int kBkBase = kConsumers + 32;      // bookkeeper warp
+constexpr int kFinBase = kConsumers + 64;     // finalizer group
+constexpr int kThreads = kFinBase + kFinThreads;
+constexpr int kFinCap = 128;                  // requests awaiting their finalize
 constexpr int kSegEl = 1024;        // inverse-CDF segment: 32 lanes x 32 elements
 constexpr int kMaxSeg = 1024;       // => V <= 2^20
 constexpr int kMaxRowsPerReq = 128;  // chain: 2K+1 <= 65; tree: N + M <= 128
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 constexpr uint64_t kWaitLimitAfterTimeoutNs = 1000000ull;  // 1 ms
 
-enum RowKind : int { KIND_ARGMAX = 0, KIND_SOFTMAX = 1, KIND_TOPK = 2 };
+static_assert(kVecPerThread * 16 * kConsumers == kChunkBytes, "chunk split");
+
+enum RowKind : int { KIND_ARGMAX = 0, KIND_SOFTMAX = 1, KIND_TOPK = 2, KIND_RESID_PASS = 3 };
 
 struct WsHeader {
   unsigned int work_counter;
   unsigned int done_ctas;
   int error;
-  int pad;
+  int n_jobs;  // residual-pass jobs left by the chain pass (reset by the residual pass)
 };
 
 // Device view of the caller's workspace.
 struct Ws {
   WsHeader* hdr;
-  unsigned int* tickets;  // [B]
-  float2* partials;       // [rows_max * ipr]
-  float* scratch;         // per-request residual rows (tree walk) [B][V]
+  unsigned int* tickets;  // [SV_MAX_B]
+  float2* partials;       // [rows_max * ipr * kConsumerWarps]
+  float* scratch;         // per-request residual rows (tree walk) [B][2][V]
+  void* jobs;             // residual-pass jobs [SV_MAX_B]
 };
 
 struct StageMeta {
@@ -54,11 +66,23 @@ struct StageMeta {
   int n_el;      // elements in this chunk
   int el_base;   // first element's index within the row
   float c_hi, c_lo;
-  const char* src;
+  const char* src;   // first element of the chunk
+  const char* src2;  // second row's chunk (residual pass), or null
+  float4 aux;        // problem-specific constants of the chunk
+  int sub;           // problem-specific small value (residual pass: mode)
+};
+
+// What the bookkeeper needs about a result slot.
+struct ResMeta {
+  int item;  // -1: no more work
+  int pos;
+  int slot;  // partial index: row * ipr + chunk
+  int kind;
+  float c_hi, c_lo;
 };
 
 struct FinScratch {
-  double dsum[kConsumerWarps];
+  double dsum[kFinWarps];
   float seg[kMaxSeg];
   float rm[kMaxRowsPerReq];
   float rz[kMaxRowsPerReq];
@@ -72,16 +96,21 @@ struct FinScratch {
   int misc[8];
 };
 
-struct Shared {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+struct __align__(16) Shared {
+  uint64_t full[kStages];      // producer -> consumers: chunk landed (tx bytes)
+  uint64_t empty[kStages];     // consumers -> producer: chunk in registers
+  uint64_t res_done[kResSlots];  // producer meta + consumer partials -> bookkeeper
+  uint64_t res_free[kResSlots];  // bookkeeper -> producer: slot consumed
   StageMeta meta[kStages];
-  MS red_ms[2][kConsumerWarps];
-  VI red_vi[2][kConsumerWarps];
-  int fin_pending;
+  ResMeta res_meta[kResSlots];
+  float2 res_part[kResSlots][kConsumerWarps];
+  int fin_q[kFinCap];
+  unsigned fin_head;           // next entry the finalizer takes (finalizer only)
+  unsigned fin_tail;           // entries published (bookkeeper only)
+  unsigned bk_done;            // the bookkeeper has booked every chunk
+  int fin_cmd;                 // finalizer group command: pos, -1 idle, -2 exit
   int n_pos;
   int timed_out;  // a bounded wait of this CTA expired: later waits are short
-  int pad;
   FinScratch fin;
 };
 
@@ -90,7 +119,7 @@ struct PosTables {
   int* info;      // request id | kind << 16 | extra << 20
   int* rstart;    // [n_pos + 1] first flat row of each position
   float2* scale;  // log2(e)/t pair per position
-  unsigned long long* aux;  // tree: referenced draft rows per position
+  float4* aux;    // problem-specific per-position data (P::kAuxBytes each)
 };
 
 __device__ __forceinline__ int info_req(int info) { return info & 0xffff; }
@@ -161,65 +190,70 @@ __device__ __forceinline__ int4 block_excl_scan4(int4 v, int4* warp_tot, int4& t
 
 // ------------------------------------------------------------ chunk reduce
 
+__device__ __forceinline__ float nan_f() { return __int_as_float(0x7fc00000); }
+
 // Fast path: bf16 chunk staged in shared memory.  Each consumer thread
-// takes up to eight 16-byte vectors, releases the stage as soon as they are
-// in registers, then reduces.
+// takes kVecPerThread 16-byte vectors, releases the stage as soon as they
+// are in registers, then reduces them with independent accumulators.
 template <int KIND>
 __device__ __forceinline__ void reduce_chunk_bf16(const StageMeta& mt, const uint4* stage,
                                                   uint64_t* empty_bar, int ctid, int lane,
                                                   MS& ms, VI& vi) {
   const int nvec = mt.n_el >> 3;
-  uint4 r[8];
+  uint4 r[kVecPerThread];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
+  for (int k = 0; k < kVecPerThread; ++k) {
     const int v = ctid + k * kConsumers;
     r[k] = v < nvec ? stage[v] : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
   }
   __syncwarp();
   if (lane == 0) mbar_arrive(empty_bar);
 
-  uint32_t mx2 = 0xff80ff80u;
+  uint32_t mk[kVecPerThread];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    mx2 = bf16x2_max_nan(mx2, r[k].x);
-    mx2 = bf16x2_max_nan(mx2, r[k].y);
-    mx2 = bf16x2_max_nan(mx2, r[k].z);
-    mx2 = bf16x2_max_nan(mx2, r[k].w);
-  }
+  for (int k = 0; k < kVecPerThread; ++k)
+    mk[k] = bf16x2_max_nan(bf16x2_max_nan(r[k].x, r[k].y), bf16x2_max_nan(r[k].z, r[k].w));
+  uint32_t mx2 = mk[0];
+#pragma unroll
+  for (int k = 1; k < kVecPerThread; ++k) mx2 = bf16x2_max_nan(mx2, mk[k]);
   const float a = bf16lo(mx2), b = bf16hi(mx2);
-  float m = (a != a || b != b) ? __int_as_float(0x7fc00000) : fmaxf(a, b);
-  if (m == kPosInf) m = __int_as_float(0x7fc00000);
+  float m = (a != a || b != b) ? nan_f() : fmaxf(a, b);
+  if (m == kPosInf) m = nan_f();
 
   if (KIND == KIND_SOFTMAX) {
     float s = 0.f;
     if (m == m && m != kNegInf) {
       const Scale2 c{mt.c_hi, mt.c_lo};
+      float sk[kVecPerThread];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < kVecPerThread; ++k) {
         const uint32_t w[4] = {r[k].x, r[k].y, r[k].z, r[k].w};
+        float acc = 0.f;
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-          s += fast_exp2(scaled_arg(bf16lo(w[h]), m, c));
-          s += fast_exp2(scaled_arg(bf16hi(w[h]), m, c));
+          acc += fast_exp2(scaled_arg(bf16lo(w[h]), m, c));
+          acc += fast_exp2(scaled_arg(bf16hi(w[h]), m, c));
         }
+        sk[k] = acc;
       }
+      s = (sk[0] + sk[1]) + (sk[2] + sk[3]);
     }
     ms = MS{m, s};
   } else {
     int idx = 0x7fffffff;
     if (m == m) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < kVecPerThread; ++k) {
         const int v = ctid + k * kConsumers;
         const uint32_t w[4] = {r[k].x, r[k].y, r[k].z, r[k].w};
+        int cand = 0x7fffffff;
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
+        for (int h = 3; h >= 0; --h) {  // descending, so the lowest match wins
           const int e = mt.el_base + v * 8 + 2 * h;
-          if (v < nvec && idx == 0x7fffffff) {
-            if (bf16lo(w[h]) == m) idx = e;
-            else if (bf16hi(w[h]) == m) idx = e + 1;
-          }
+          if (bf16hi(w[h]) == m) cand = e + 1;
+          if (bf16lo(w[h]) == m) cand = e;
         }
+        if (v < nvec) idx = min(idx, cand);
       }
     }
     vi = VI{m, idx};
@@ -255,12 +289,40 @@ __device__ __forceinline__ void reduce_chunk_generic(const StageMeta& mt, const 
       const Scale2 c{mt.c_hi, mt.c_lo};
       for (int e = ctid; e < mt.n_el; e += kConsumers) s += fast_exp2(scaled_arg(ld(e), m, c));
     }
-    ms = bad ? MS{__int_as_float(0x7fc00000), 0.f} : MS{m, s};
+    ms = bad ? MS{nan_f(), 0.f} : MS{m, s};
   } else {
-    vi = bad ? VI{__int_as_float(0x7fc00000), 0} : VI{m, idx};
+    vi = bad ? VI{nan_f(), 0} : VI{m, idx};
   }
   __syncwarp();
   if (lane == 0) mbar_arrive(empty_bar);
+}
+
+// A logit-row chunk reduced by one consumer warp: (max, sum exp) for
+// sampled rows, (max, lowest argmax) for greedy rows, warp-reduced.
+__device__ __forceinline__ float2 reduce_row_chunk(const StageMeta& mt, const unsigned char* sp,
+                                                   uint64_t* empty_bar, int ctid, int lane,
+                                                   bool bulk, int es) {
+  MS ms{kNegInf, 0.f};
+  VI vi{kNegInf, 0x7fffffff};
+  const bool fast = bulk && es == 2;
+  if (mt.kind == KIND_ARGMAX) {
+    if (fast)
+      reduce_chunk_bf16<KIND_ARGMAX>(mt, reinterpret_cast<const uint4*>(sp), empty_bar, ctid,
+                                     lane, ms, vi);
+    else
+      reduce_chunk_generic<KIND_ARGMAX>(mt, reinterpret_cast<const char*>(sp), bulk, es,
+                                        empty_bar, ctid, lane, ms, vi);
+    vi = warp_reduce_vi(vi);
+    return make_float2(vi.v, __int_as_float(vi.i));
+  }
+  if (fast)
+    reduce_chunk_bf16<KIND_SOFTMAX>(mt, reinterpret_cast<const uint4*>(sp), empty_bar, ctid,
+                                    lane, ms, vi);
+  else
+    reduce_chunk_generic<KIND_SOFTMAX>(mt, reinterpret_cast<const char*>(sp), bulk, es,
+                                       empty_bar, ctid, lane, ms, vi);
+  ms = warp_reduce_ms(ms, Scale2{mt.c_hi, mt.c_lo});
+  return make_float2(ms.m, ms.s);
 }
 
 // ---------------------------------------------------------- inverse CDF
@@ -276,7 +338,7 @@ template <class WF>
 __device__ int icdf_draw(int V, double u, const WF& wf, FinScratch& fs, int ctid) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int nseg = (V + kSegEl - 1) / kSegEl;
-  for (int s = warp; s < nseg; s += kConsumerWarps) {
+  for (int s = warp; s < nseg; s += kFinWarps) {
     float w[32];
     wf(s * kSegEl + lane * 32, w);
     float ls = 0.f;
@@ -285,7 +347,7 @@ __device__ int icdf_draw(int V, double u, const WF& wf, FinScratch& fs, int ctid
     const float inc = warp_incl_scan(ls, lane);
     if (lane == 31) fs.seg[s] = inc;
   }
-  named_sync(1, kConsumers);
+  named_sync(1, kFinThreads);
   if (warp == 0) {
     const int per = (nseg + 31) / 32;
     const int lo = min(lane * per, nseg), hi = min(lo + per, nseg);
@@ -372,9 +434,9 @@ __device__ int icdf_draw(int V, double u, const WF& wf, FinScratch& fs, int ctid
       fs.token = -1;
     }
   }
-  named_sync(1, kConsumers);
+  named_sync(1, kFinThreads);
   const int tok = fs.token;
-  named_sync(1, kConsumers);
+  named_sync(1, kFinThreads);
   return tok;
 }
 

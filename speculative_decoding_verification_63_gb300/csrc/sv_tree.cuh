@@ -17,7 +17,7 @@
 namespace sv {
 
 struct TreeProblem {
-  static constexpr bool kAux = true;
+  static constexpr int kAuxBytes = 8;
   int n_req, N, M, V, max_depth, es, ipr, chunk_el, max_topk;
   bool bulk;
   const char* target;
@@ -106,7 +106,7 @@ struct TreeProblem {
         lrow += kind < 0 ? 0 : nn;
       }
       tab.info[pos] = make_info(b, kind < 0 ? 0 : kind, kind < 0 ? 0 : nn);
-      tab.aux[pos] = mask;
+      reinterpret_cast<unsigned long long*>(tab.aux)[pos] = mask;
       const Scale2 c = scale_for(temperature[b]);
       tab.scale[pos] = make_float2(c.hi, c.lo);
       if (kind < 0 && blockIdx.x == 0) write_failed(b, 0x20);
@@ -117,23 +117,37 @@ struct TreeProblem {
     }
   }
 
-  __device__ const char* row_ptr(const PosTables& tab, int pos, int rl, int& kind,
-                                 Scale2& c) const {
-    const int info = tab.info[pos];
+  __device__ void fill_stage(const PosTables& tab, int rl, StageMeta& mt) const {
+    const int info = tab.info[mt.pos];
     const int b = info_req(info), nn = info_extra(info);
-    kind = info_kind(info);
-    const float2 s = tab.scale[pos];
-    c.hi = s.x;
-    c.lo = s.y;
-    if (rl < nn) return target + (static_cast<int64_t>(b) * N + rl) * t_stride;
-    // the (rl - nn)-th referenced draft row
-    unsigned long long m = tab.aux[pos];
-    for (int k = rl - nn; k > 0; --k) m &= m - 1;
-    const int r = __ffsll(static_cast<long long>(m)) - 1;
-    return draft + (static_cast<int64_t>(b) * M + r) * d_stride;
+    mt.kind = info_kind(info);
+    const float2 s = tab.scale[mt.pos];
+    mt.c_hi = s.x;
+    mt.c_lo = s.y;
+    const char* rp;
+    if (rl < nn) {
+      rp = target + (static_cast<int64_t>(b) * N + rl) * t_stride;
+    } else {
+      // the (rl - nn)-th referenced draft row
+      unsigned long long m = ref_of(tab, mt.pos);
+      for (int k = rl - nn; k > 0; --k) m &= m - 1;
+      const int r = __ffsll(static_cast<long long>(m)) - 1;
+      rp = draft + (static_cast<int64_t>(b) * M + r) * d_stride;
+    }
+    mt.src = rp + static_cast<size_t>(mt.el_base) * es;
   }
 
-  __device__ void finalize(Shared& sh, const PosTables& tab, int pos, int ctid) const;
+  __device__ float2 consume(const StageMeta& mt, const unsigned char* sp, uint64_t* empty_bar,
+                            int ctid, int lane) const {
+    return reduce_row_chunk(mt, sp, empty_bar, ctid, lane, bulk, es);
+  }
+
+  __device__ static unsigned long long ref_of(const PosTables& tab, int pos) {
+    return reinterpret_cast<const unsigned long long*>(tab.aux)[pos];
+  }
+
+  __device__ void finalize(Shared& sh, const PosTables& tab, int pos, int ftid) const;
+  __device__ void last_cta_reset() const {}
 };
 
 // Weights for the tree's inverse-CDF draw: either p_node (unnormalised
@@ -159,12 +173,12 @@ struct TreeWeights {
 };
 
 __device__ void TreeProblem::finalize(Shared& sh, const PosTables& tab, int pos,
-                                      int ctid) const {
+                                      int ftid) const {
   FinScratch& fs = sh.fin;
-  const int warp = ctid >> 5, lane = ctid & 31;
+  const int warp = ftid >> 5, lane = ftid & 31;
   const int info = tab.info[pos];
   const int b = info_req(info), kind = info_kind(info), nn = info_extra(info);
-  const unsigned long long mask = tab.aux[pos];
+  const unsigned long long mask = ref_of(tab, pos);
   const int r0 = tab.rstart[pos];
   const int nrows = tab.rstart[pos + 1] - r0;
   const Scale2 c{tab.scale[pos].x, tab.scale[pos].y};
@@ -174,40 +188,57 @@ __device__ void TreeProblem::finalize(Shared& sh, const PosTables& tab, int pos,
   const int* par = parent + static_cast<size_t>(b) * N;
   const int* qr = q_row + static_cast<size_t>(b) * N;
 
-  // (1) merge chunk partials of every row
-  for (int j = warp; j < nrows; j += kConsumerWarps) {
-    const float2* pp = ws.partials + static_cast<size_t>(r0 + j) * ipr;
-    if (greedy) {
-      VI v{kNegInf, 0x7fffffff};
-      for (int ch = lane; ch < ipr; ch += 32) {
-        const float2 t = __ldcg(pp + ch);
-        v = vi_better(v, VI{t.x, __float_as_int(t.y)});
-      }
-      v = warp_reduce_vi(v);
-      if (lane == 0) {
-        fs.rm[j] = v.v;
-        fs.ridx[j] = v.i;
-      }
-    } else {
-      MS v{kNegInf, 0.f};
-      for (int ch = lane; ch < ipr; ch += 32) {
-        const float2 t = __ldcg(pp + ch);
-        v = ms_combine(v, MS{t.x, t.y}, c);
-      }
-      v = warp_reduce_ms(v, c);
-      if (lane == 0) {
-        fs.rm[j] = v.m;
-        fs.rz[j] = v.s;
+  // (1) merge the chunk partials of every row: a warp takes 32 / ipr rows
+  // per pass, one group of ipr lanes per row (all loads issued first), then
+  // a guarded shfl_down tree within each group
+  {
+    const int width = ipr <= 32 ? ipr : 32;
+    const int rpw = 32 / width;
+    const int g = lane / width, r = lane % width;
+    for (int j0 = warp * rpw; j0 < nrows; j0 += kFinWarps * rpw) {
+      const int j = j0 + g;
+      const bool own = g < rpw && j < nrows;
+      const float2* pp = ws.partials + static_cast<size_t>(r0 + (own ? j : 0)) * ipr;
+      if (greedy) {
+        VI v{kNegInf, 0x7fffffff};
+        if (own)
+          for (int ch = r; ch < ipr; ch += width) {
+            const float2 u = __ldcg(pp + ch);
+            v = vi_better(v, VI{u.x, __float_as_int(u.y)});
+          }
+        for (int o = 1; o < width; o <<= 1) {
+          const VI w{__shfl_down_sync(0xffffffffu, v.v, o), __shfl_down_sync(0xffffffffu, v.i, o)};
+          if (r + o < width) v = vi_better(v, w);
+        }
+        if (own && r == 0) {
+          fs.rm[j] = v.v;
+          fs.ridx[j] = v.i;
+        }
+      } else {
+        MS v{kNegInf, 0.f};
+        if (own)
+          for (int ch = r; ch < ipr; ch += width) {
+            const float2 u = __ldcg(pp + ch);
+            v = ms_combine(v, MS{u.x, u.y}, c);
+          }
+        for (int o = 1; o < width; o <<= 1) {
+          const MS w{__shfl_down_sync(0xffffffffu, v.m, o), __shfl_down_sync(0xffffffffu, v.s, o)};
+          if (r + o < width) v = ms_combine(v, w, c);
+        }
+        if (own && r == 0) {
+          fs.rm[j] = v.m;
+          fs.rz[j] = v.s;
+        }
       }
     }
   }
-  if (ctid == 0) fs.err = 0;
-  named_sync(1, kConsumers);
+  if (ftid == 0) fs.err = 0;
+  named_sync(1, kFinThreads);
 
   // (2) validate the tree and the row statistics
   {
     int err = 0;
-    for (int cc = ctid; cc < nn; cc += kConsumers) {
+    for (int cc = ftid; cc < nn; cc += kFinThreads) {
       if (cc == 0) {
         if (par[0] != -1) err |= 0x08;
         continue;
@@ -228,13 +259,13 @@ __device__ void TreeProblem::finalize(Shared& sh, const PosTables& tab, int pos,
       }
       if (d > max_depth) err |= 0x08;
     }
-    for (int j = ctid; j < nrows; j += kConsumers) {
+    for (int j = ftid; j < nrows; j += kFinThreads) {
       if (fs.rm[j] != fs.rm[j]) err |= 0x02;
       else if (fs.rm[j] == kNegInf || (!greedy && !(fs.rz[j] > 0.f))) err |= 0x04;
     }
     if (err) atomicOr(&fs.err, err);
   }
-  named_sync(1, kConsumers);
+  named_sync(1, kFinThreads);
   int err = fs.err;
 
   int L = 0, node = 0, token = -1;
@@ -263,7 +294,7 @@ __device__ void TreeProblem::finalize(Shared& sh, const PosTables& tab, int pos,
         s_w = 0.0;
       }
     }
-    named_sync(1, kConsumers);
+    named_sync(1, kFinThreads);
     const int nc = n_children;
     if (greedy) {
       const int a = fs.ridx[node];
@@ -277,10 +308,10 @@ __device__ void TreeProblem::finalize(Shared& sh, const PosTables& tab, int pos,
         token = a;
         break;
       }
-      if (ctid == 0) path[L] = next;
+      if (ftid == 0) path[L] = next;
       ++L;
       node = next;
-      named_sync(1, kConsumers);
+      named_sync(1, kFinThreads);
       continue;
     }
     const char* prow = target + (static_cast<int64_t>(b) * N + node) * t_stride;
@@ -294,7 +325,7 @@ __device__ void TreeProblem::finalize(Shared& sh, const PosTables& tab, int pos,
       const float mq = fs.rm[jq], zq = fs.rz[jq];
       const float* wsrc = ws.scratch + (static_cast<size_t>(b) * 2 + w_cur) * V;
       float* wdst = ws.scratch + (static_cast<size_t>(b) * 2 + (w_cur ^ 1)) * V;
-      if (ctid == 0) {
+      if (ftid == 0) {
         // accept test of child ch against the current residual r
         const int x = tok[ch];
         const double q = exp2(static_cast<double>(load_logit(qrow, es, x) - mq) * cd) /
@@ -307,7 +338,7 @@ __device__ void TreeProblem::finalize(Shared& sh, const PosTables& tab, int pos,
         const double u = static_cast<double>(u_accept[static_cast<size_t>(b) * N + ch]);
         decision = u * q < r;
       }
-      named_sync(1, kConsumers);
+      named_sync(1, kFinThreads);
       if (decision) {
         next = ch;
         break;
@@ -317,7 +348,7 @@ __device__ void TreeProblem::finalize(Shared& sh, const PosTables& tab, int pos,
       const float inv_sw = w_mode == 0 ? 0.f : static_cast<float>(1.0 / s_w);
       const int mode = w_mode;
       float part = 0.f;
-      for (int t = ctid; t < V; t += kConsumers) {
+      for (int t = ftid; t < V; t += kFinThreads) {
         const float rt = mode == 0 ? fast_exp2(scaled_arg(load_logit(prow, es, t), mp, c)) * izp
                                    : __ldcg(wsrc + t) * inv_sw;
         const float qt = fast_exp2(scaled_arg(load_logit(qrow, es, t), mq, c)) * izq;
@@ -329,23 +360,23 @@ __device__ void TreeProblem::finalize(Shared& sh, const PosTables& tab, int pos,
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) dp += __shfl_xor_sync(0xffffffffu, dp, o);
       if (lane == 0) fs.dsum[warp] = dp;
-      named_sync(1, kConsumers);
-      if (ctid == 0) {
+      named_sync(1, kFinThreads);
+      if (ftid == 0) {
         double S = 0.0;
-        for (int w = 0; w < kConsumerWarps; ++w) S += fs.dsum[w];
+        for (int w = 0; w < kFinWarps; ++w) S += fs.dsum[w];
         if (S > 0.0) {  // zero mass (rounding only) keeps r as it was
           s_w = S;
           w_mode = 1;
           w_cur ^= 1;
         }
       }
-      named_sync(1, kConsumers);
+      named_sync(1, kFinThreads);
     }
     if (next >= 0) {
-      if (ctid == 0) path[L] = next;
+      if (ftid == 0) path[L] = next;
       ++L;
       node = next;
-      named_sync(1, kConsumers);
+      named_sync(1, kFinThreads);
       continue;
     }
     // a leaf, or every child rejected: draw from r with u_sample
@@ -357,13 +388,13 @@ __device__ void TreeProblem::finalize(Shared& sh, const PosTables& tab, int pos,
     wf.es = es;
     wf.V = V;
     wf.vec_ok = bulk;
-    token = icdf_draw(V, static_cast<double>(u_sample[b]), wf, fs, ctid);
+    token = icdf_draw(V, static_cast<double>(u_sample[b]), wf, fs, ftid);
     if (token < 0) err |= 0x04;
     break;
   }
 
   // outputs
-  for (int i = ctid; i <= max_depth; i += kConsumers) {
+  for (int i = ftid; i <= max_depth; i += kFinThreads) {
     int v = -1;
     if (!err) {
       if (i < L) v = tok[path[i]];
@@ -371,15 +402,15 @@ __device__ void TreeProblem::finalize(Shared& sh, const PosTables& tab, int pos,
     }
     out_tokens[static_cast<size_t>(b) * (max_depth + 1) + i] = v;
   }
-  for (int i = ctid; i < max_depth; i += kConsumers)
+  for (int i = ftid; i < max_depth; i += kFinThreads)
     accepted_nodes[static_cast<size_t>(b) * max_depth + i] = (!err && i < L) ? path[i] : -1;
-  if (ctid == 0) {
+  if (ftid == 0) {
     out_len[b] = err ? 0 : L + 1;
     accept_len[b] = err ? 0 : L;
     if (err) record_error(&ws.hdr->error, err);
     ws.tickets[b] = 0u;
   }
-  named_sync(1, kConsumers);
+  named_sync(1, kFinThreads);
 }
 
 }  // namespace sv

@@ -17,8 +17,8 @@ def test_toy_chain_10000_rounds():
     """Toy workload (B=4, K=4, V=5 fp32): 10,000 rounds of 4 requests, run
     as one batch of 40,000 independent requests."""
     total = dict(requests=0, exact=0, near_accept=0, near_draw=0)
-    for r in range(10):
-        inp = wl.make_chain(1, B=4000, seed=wl.SEED_BASE + 1 + 1000 * r)
+    for r in range(40):
+        inp = wl.make_chain(1, B=1000, seed=wl.SEED_BASE + 1 + 1000 * r)
         st, got, _ = check_chain(inp)
         for k in total:
             total[k] += st[k]
@@ -30,6 +30,14 @@ def test_toy_chain_10000_rounds():
 def test_small_chain_many_seeds():
     """Small-chain workload (K=4, V=32000 bf16, peaked target): 64 requests."""
     check_chain(wl.make_chain(2, B=64))
+
+
+@pytest.mark.parametrize("B", [1, 3, 7])
+def test_small_chain_odd_batches(B):
+    """The small-chain workload as specified (B=1) and other odd batch sizes
+    (per-request tables of odd length in shared memory)."""
+    for seed in range(3):
+        check_chain(wl.make_chain(2, B=B, seed=wl.SEED_BASE + 2 + 17 * seed + B))
 
 
 def test_headline_full_size():
@@ -100,7 +108,7 @@ def test_no_drafts_is_plain_sampling():
 
 
 def test_many_requests():
-    check_chain(wl.make_chain(2, B=1500, K=3, V=64, seed=13))
+    check_chain(wl.make_chain(2, B=1024, K=3, V=64, seed=13))
 
 
 def test_workspace_reuse_gives_same_result():

@@ -19,6 +19,10 @@ def test_tree_workload_full_size():
     assert got["out_len"].min() >= 1
 
 
+def test_tree_odd_batch():
+    check_tree(wl.make_tree(B=5, seed=46))
+
+
 def test_tree_greedy_deep_walks():
     inp = wl.make_tree(B=16, temperature=0.0, greedy_hint=0.8, seed=41)
     st, got, ref = check_tree(inp)
