@@ -7,7 +7,6 @@
 
 #include "specverify.h"
 #include "sv_chain.cuh"
-#include "sv_resid.cuh"
 #include "sv_tree.cuh"
 
 namespace {
@@ -18,19 +17,26 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 struct Layout {
-  size_t tickets, jobs, partials, scratch, total;
+  size_t tickets, draws, jobs, partials, segsums, scratch, total;
 };
 
-// The header and the per-request tickets sit at fixed offsets with a fixed
-// capacity (SV_MAX_B), so the region that every call leaves zeroed is the
-// same for all problem sizes: one initialised workspace serves chain and
-// tree calls of any shape, one call at a time.
-Layout layout_for(int64_t /*B*/, int64_t rows_max, int64_t ipr, int64_t scratch_floats) {
+static_assert(kDrawTicketBase == SV_MAX_B, "draw tickets follow the request tickets");
+static_assert(SV_MAX_V / kRSeg <= kMaxPages * kPageSeg && 2 * kMaxPages <= kMaxRowsPerReq,
+              "draw finalize pages");
+
+// The header, the tickets (requests, then their draws) and the draw list
+// sit at fixed offsets with a fixed capacity (SV_MAX_B), so the region that
+// every call leaves zeroed is the same for all problem sizes: one
+// initialised workspace serves chain and tree calls of any shape, one call
+// at a time.
+Layout layout_for(int64_t partial_slots, int64_t segsum_floats, int64_t scratch_floats) {
   Layout L;
   L.tickets = align_up(sizeof(WsHeader));
-  L.jobs = align_up(L.tickets + sizeof(unsigned int) * static_cast<size_t>(SV_MAX_B));
-  L.partials = align_up(L.jobs + sizeof(ResidJob) * static_cast<size_t>(SV_MAX_B));
-  L.scratch = align_up(L.partials + sizeof(float2) * static_cast<size_t>(rows_max * ipr));
+  L.draws = align_up(L.tickets + sizeof(unsigned int) * 2 * static_cast<size_t>(SV_MAX_B));
+  L.jobs = align_up(L.draws + sizeof(int) * static_cast<size_t>(SV_MAX_B));
+  L.partials = align_up(L.jobs + sizeof(P2Job) * static_cast<size_t>(SV_MAX_B));
+  L.segsums = align_up(L.partials + sizeof(float2) * static_cast<size_t>(partial_slots));
+  L.scratch = align_up(L.segsums + sizeof(float) * static_cast<size_t>(segsum_floats));
   L.total = align_up(L.scratch + sizeof(float) * static_cast<size_t>(scratch_floats));
   return L;
 }
@@ -40,7 +46,9 @@ Ws ws_view(void* base, const Layout& L) {
   Ws w;
   w.hdr = reinterpret_cast<WsHeader*>(p);
   w.tickets = reinterpret_cast<unsigned int*>(p + L.tickets);
+  w.draws = reinterpret_cast<int*>(p + L.draws);
   w.partials = reinterpret_cast<float2*>(p + L.partials);
+  w.segsums = reinterpret_cast<float*>(p + L.segsums);
   w.jobs = reinterpret_cast<void*>(p + L.jobs);
   w.scratch = reinterpret_cast<float*>(p + L.scratch);
   return w;
@@ -50,13 +58,17 @@ int es_of(sv_dtype d) { return d == SV_BF16 ? 2 : 4; }
 int chunk_el_of(sv_dtype d) { return kChunkBytes / es_of(d); }
 int resid_chunk_el_of(sv_dtype d) { return kChunkBytes / 2 / es_of(d); }
 
-// Chain calls: the chain pass stores per-row chunk partials, the residual
-// pass per-job segment sums, in the same region (the passes run in turn).
+// Chain calls: per-row chunk partials for the main pass, per-request
+// segment sums for the draw pass.
 Layout chain_layout(int64_t B, int64_t K, int64_t V, sv_dtype dtype) {
   const int64_t ipr = (V + chunk_el_of(dtype) - 1) / chunk_el_of(dtype);
   const int64_t ipr2 = (V + resid_chunk_el_of(dtype) - 1) / resid_chunk_el_of(dtype);
-  const int64_t slots = std::max(B * (2 * K + 1) * ipr, B * ipr2 * kConsumerWarps);
-  return layout_for(B, slots, 1, 0);
+  return layout_for(B * (2 * K + 1) * ipr, B * ipr2 * (resid_chunk_el_of(dtype) / kRSeg), 0);
+}
+
+Layout tree_layout(int64_t B, int64_t N, int64_t M, int64_t V, sv_dtype dtype) {
+  const int64_t ipr = (V + chunk_el_of(dtype) - 1) / chunk_el_of(dtype);
+  return layout_for(B * (N + M) * ipr, 0, B * 2 * V);
 }
 
 // Per-device facts, looked up once.
@@ -161,9 +173,7 @@ size_t sv_tree_workspace_bytes(int32_t B, int32_t N, int32_t M, int32_t V, sv_dt
       M > SV_MAX_TREE_NODES || V < 1 || V > SV_MAX_V || (dtype != SV_BF16 && dtype != SV_FP32) ||
       max_top_k < 0 || max_top_k > SV_MAX_TOPK)
     return 0;
-  const int64_t ipr = (V + chunk_el_of(dtype) - 1) / chunk_el_of(dtype);
-  return layout_for(B, static_cast<int64_t>(B) * (N + M), ipr, static_cast<int64_t>(B) * 2 * V)
-      .total;
+  return tree_layout(B, N, M, V, dtype).total;
 }
 
 sv_status sv_workspace_init(void* workspace, size_t ws_bytes, sv_stream_t stream) {
@@ -227,36 +237,13 @@ sv_status sv_verify_chain(const sv_chain_args* a, void* workspace, size_t ws_byt
   p.p_at = a->p_at_draft;
   p.q_at = a->q_at_draft;
   p.ws = ws_view(workspace, L);
-  p.jobs = static_cast<ResidJob*>(p.ws.jobs);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  p.jobs = static_cast<P2Job*>(p.ws.jobs);
+  p.chunk2 = resid_chunk_el_of(a->dtype);
+  p.ipr2 = (a->V + p.chunk2 - 1) / p.chunk2;
 
   const int64_t items_max = static_cast<int64_t>(a->B) * (2 * a->K + 1) * ipr;
   const int grid = static_cast<int>(std::min<int64_t>(std::max<int64_t>(items_max, 1), dev.sms));
-  sv_status st = launch(p, grid, s);
-  if (st != SV_OK) return st;
-
-  // residual / bonus draws of the sampled requests, over the whole GPU
-  ResidProblem r;
-  r.n_req = a->B;
-  r.K = a->K;
-  r.V = a->V;
-  r.es = es;
-  r.chunk_el = resid_chunk_el_of(a->dtype);
-  r.ipr = (a->V + r.chunk_el - 1) / r.chunk_el;
-  r.bulk = p.bulk;
-  r.target = p.target;
-  r.t_stride = p.t_stride;
-  r.draft = p.draft;
-  r.d_stride = p.d_stride;
-  r.uniforms = a->uniforms;
-  r.out_tokens = a->out_tokens;
-  r.out_len = a->out_len;
-  r.accept_len = a->accept_len;
-  r.jobs = p.jobs;
-  r.ws = p.ws;
-  const int64_t items2 = static_cast<int64_t>(a->B) * r.ipr;
-  const int grid2 = static_cast<int>(std::min<int64_t>(std::max<int64_t>(items2, 1), dev.sms));
-  return launch(r, grid2, s);
+  return launch(p, grid, reinterpret_cast<cudaStream_t>(stream));
 }
 
 sv_status sv_verify_tree(const sv_tree_args* a, void* workspace, size_t ws_bytes,
@@ -285,8 +272,7 @@ sv_status sv_verify_tree(const sv_tree_args* a, void* workspace, size_t ws_bytes
   const int es = es_of(a->dtype);
   const int chunk_el = chunk_el_of(a->dtype);
   const int ipr = (a->V + chunk_el - 1) / chunk_el;
-  const Layout L = layout_for(a->B, static_cast<int64_t>(a->B) * (a->N + a->M), ipr,
-                              static_cast<int64_t>(a->B) * 2 * a->V);
+  const Layout L = tree_layout(a->B, a->N, a->M, a->V, a->dtype);
   TreeProblem p;
   p.n_req = a->B;
   p.N = a->N;

@@ -7,15 +7,35 @@
 // from norm(max(0, p_n - q_n)) -- or, if all drafts pass, from p_{nd} --
 // by inverse CDF with u_K.  Greedy requests (t == 0) accept iff x_i is the
 // argmax of target row i (lecture notes sec. 2.2; study notes sec. 10).
+//
+// Inside the persistent kernel (sv_kernel.cuh):
+//   main pass   every row the step reads is reduced chunk by chunk to
+//               (max, sum exp) or (max, lowest argmax);
+//   request     when a request's last chunk is booked, one finalizer warp
+//   finalize    merges its rows, runs the accept tests and the
+//               prefix-terminating scan, writes the accepted prefix; a
+//               greedy request is then complete, a sampled one publishes
+//               its draw (row pair n) in the global draw list;
+//   draw pass   claims beyond the main pass stream the published row pairs
+//               again as draw chunks (16 KB of p_n | 16 KB of q_n), spread
+//               over all CTAs; each consumer warp turns its 256-token
+//               segments into residual weights and their sums;
+//   draw        when the draw's last chunk is booked, one finalizer warp
+//   finalize    takes the fp64 prefix over the segment sums, finds the
+//               segment holding u * S, rescans it with bit-identical
+//               arithmetic and writes the emitted token.
 #pragma once
 
-#include "sv_resid.cuh"
+#include "sv_kernel.cuh"
 
 namespace sv {
 
 struct ChainProblem {
   static constexpr int kAuxBytes = 0;
+  static constexpr bool kWarpFinalize = true;
+  static constexpr bool kHasDraws = true;
   int n_req, K, V, es, ipr, chunk_el, max_topk;
+  int ipr2, chunk2;  // draw pass: chunks per row pair, tokens per chunk
   bool bulk;
   const char* target;
   int64_t t_stride;  // bytes between target rows
@@ -31,7 +51,7 @@ struct ChainProblem {
   int* accept_len;
   float* p_at;
   float* q_at;
-  ResidJob* jobs;  // sampled requests leave their residual / bonus draw here
+  P2Job* jobs;  // [SV_MAX_B] the draw of request b
   Ws ws;
 
   // kind of request b, or -1 if its scalar arguments are invalid
@@ -57,14 +77,14 @@ struct ChainProblem {
     record_error(&ws.hdr->error, flag);
   }
 
-  // Processing order: sampled unfiltered requests first (their finalize
-  // streams a row pair and should overlap the rest of the pass), then
-  // filtered and greedy ones.  rows: greedy nd+1, sampled 2nd+1.
+  // Processing order: sampled requests first (their draw pass should overlap
+  // the rest of the main pass), then greedy ones.  rows: greedy nd+1,
+  // sampled 2nd+1.
   __device__ void preamble(Shared& sh, PosTables& tab, int4* scan_tmp) const {
     const int per = (n_req + kThreads - 1) / kThreads;
     const int lo = min(static_cast<int>(threadIdx.x) * per, n_req);
     const int hi = min(lo + per, n_req);
-    int4 cnt = make_int4(0, 0, 0, 0);  // heavy n, heavy rows, light n, light rows
+    int4 cnt = make_int4(0, 0, 0, 0);  // sampled n, sampled rows, other n, other rows
     for (int b = lo; b < hi; ++b) {
       int nd;
       const int kind = classify(b, nd);
@@ -102,66 +122,247 @@ struct ChainProblem {
       tab.info[pos] = make_info(b, kind < 0 ? 0 : kind, nd < 0 ? 0 : min(nd, 0x7ff));
       const Scale2 c = scale_for(temperature[b]);
       tab.scale[pos] = make_float2(c.hi, c.lo);
-      if (kind < 0 && blockIdx.x == 0) write_failed(b, 0x20);
+      if (kind < 0 && blockIdx.x == 0) {
+        write_failed(b, 0x20);
+        atomicAdd(&ws.hdr->fin_count, 1u);  // never finalized: counted here
+      }
     }
     if (threadIdx.x == 0) {
       tab.rstart[n_req] = tot.y + tot.w;
       sh.n_pos = n_req;
+      sh.n_draw_cap = tot.x;
     }
   }
 
-  __device__ void fill_stage(const PosTables& tab, int rl, StageMeta& mt) const {
+  __device__ const char* trow(int b, int i) const {
+    return target + (static_cast<int64_t>(b) * (K + 1) + i) * t_stride;
+  }
+  __device__ const char* drow(int b, int i) const {
+    return draft + (static_cast<int64_t>(b) * K + i) * d_stride;
+  }
+
+  __device__ void fill_stage(const PosTables& tab, int rl, StageMeta& mt, ResMeta& rm) const {
     const int info = tab.info[mt.pos];
     const int b = info_req(info), nd = info_extra(info);
     mt.kind = info_kind(info);
     const float2 s = tab.scale[mt.pos];
     mt.c_hi = s.x;
     mt.c_lo = s.y;
-    const char* rp = rl <= nd ? target + (static_cast<int64_t>(b) * (K + 1) + rl) * t_stride
-                              : draft + (static_cast<int64_t>(b) * K + (rl - nd - 1)) * d_stride;
+    const char* rp = rl <= nd ? trow(b, rl) : drow(b, rl - nd - 1);
     mt.src = rp + static_cast<size_t>(mt.el_base) * es;
+    rm.tkt = b;
+    rm.need = (tab.rstart[mt.pos + 1] - tab.rstart[mt.pos]) * ipr;
+    rm.fin_code = mt.pos;
   }
 
-  __device__ float2 consume(const StageMeta& mt, const unsigned char* sp, uint64_t* empty_bar,
+  __device__ P2Job load_job(int b) const {
+    P2Job j;
+    const P2Job* g = jobs + b;
+    j.b = __ldcg(&g->b);
+    j.n = __ldcg(&g->n);
+    j.mode = __ldcg(&g->mode);
+    j.mp = __ldcg(&g->mp);
+    j.izp = __ldcg(&g->izp);
+    j.mq = __ldcg(&g->mq);
+    j.izq = __ldcg(&g->izq);
+    j.c_hi = __ldcg(&g->c_hi);
+    j.c_lo = __ldcg(&g->c_lo);
+    return j;
+  }
+
+  // segments of kRSeg tokens per draw chunk; a consumer warp takes
+  // segs_per_chunk / kGroupWarps of them (kSpwBf16 or kSpwF32)
+  __device__ int segs_per_chunk() const { return chunk2 / kRSeg; }
+
+  __device__ void fill_resid(const P2Job& jb, int chunk, StageMeta& mt, ResMeta& rm) const {
+    mt.kind = KIND_RESID_PASS;
+    mt.el_base = chunk * chunk2;
+    mt.n_el = min(chunk2, V - mt.el_base);
+    mt.c_hi = jb.c_hi;
+    mt.c_lo = jb.c_lo;
+    mt.aux = make_float4(jb.mp, jb.izp, jb.mq, jb.izq);
+    mt.sub = jb.mode;
+    mt.src = trow(jb.b, jb.n) + static_cast<size_t>(mt.el_base) * es;
+    mt.src2 = jb.mode == 0 ? drow(jb.b, jb.n) + static_cast<size_t>(mt.el_base) * es : nullptr;
+    rm.slot = (jb.b * ipr2 + chunk) * segs_per_chunk();
+    rm.tkt = kDrawTicketBase + jb.b;
+    rm.need = ipr2;
+    rm.fin_code = jb.b | kFinResid;
+  }
+
+  // draw pass: warp w of the group reduces segments w * spw + s (s < spw)
+  // of the chunk, lane l tokens [8 l, 8 l + 8) of each; returns the
+  // segment sums.  Staged data is held packed until the stage is released.
+  __device__ float4 consume_resid(const StageMeta& mt, const unsigned char* sp,
+                                  uint64_t* empty_bar, int ctid, int lane) const {
+    const int warp = ctid >> 5;
+    const int spw = segs_per_chunk() / kGroupWarps;  // kSpwBf16 or kSpwF32
+    const int mode = mt.sub;
+    const ResidParams r{mt.aux.x, mt.aux.y, mt.aux.z, mt.aux.w, Scale2{mt.c_hi, mt.c_lo}, mode};
+    float tot[4] = {0.f, 0.f, 0.f, 0.f};
+    auto seg_sum = [&](const float* xp, const float* xq, int t0) {
+      float w[8];
+      const float ls = resid_weights8(xp, xq, t0, mt.n_el, r, w);
+      return __shfl_sync(0xffffffffu, warp_incl_scan_rn(ls, lane), 31);
+    };
+    const char* pb = reinterpret_cast<const char*>(sp);
+    const char* qb = pb + kChunkBytes / 2;
+    if (bulk && es == 2) {
+      uint4 pv[kSpwBf16], qv[kSpwBf16];
+#pragma unroll
+      for (int s = 0; s < kSpwBf16; ++s) {
+        const int t0 = (warp * kSpwBf16 + s) * kRSeg + lane * 8;
+        pv[s] = *reinterpret_cast<const uint4*>(pb + t0 * 2);
+        qv[s] = mode == 0 ? *reinterpret_cast<const uint4*>(qb + t0 * 2) : make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar);
+#pragma unroll
+      for (int s = 0; s < kSpwBf16; ++s) {
+        const int t0 = (warp * kSpwBf16 + s) * kRSeg + lane * 8;
+        float xp[8], xq[8];
+        const uint32_t wp[4] = {pv[s].x, pv[s].y, pv[s].z, pv[s].w};
+        const uint32_t wq[4] = {qv[s].x, qv[s].y, qv[s].z, qv[s].w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          xp[2 * h] = bf16lo(wp[h]);
+          xp[2 * h + 1] = bf16hi(wp[h]);
+          xq[2 * h] = mode == 0 ? bf16lo(wq[h]) : kNegInf;
+          xq[2 * h + 1] = mode == 0 ? bf16hi(wq[h]) : kNegInf;
+        }
+        tot[s] = seg_sum(xp, xq, t0);
+      }
+    } else if (bulk) {
+      float4 pv[kSpwF32][2], qv[kSpwF32][2];
+#pragma unroll
+      for (int s = 0; s < kSpwF32; ++s) {
+        const int t0 = (warp * kSpwF32 + s) * kRSeg + lane * 8;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          pv[s][h] = *reinterpret_cast<const float4*>(pb + t0 * 4 + 16 * h);
+          qv[s][h] = mode == 0 ? *reinterpret_cast<const float4*>(qb + t0 * 4 + 16 * h)
+                               : make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar);
+#pragma unroll
+      for (int s = 0; s < kSpwF32; ++s) {
+        const int t0 = (warp * kSpwF32 + s) * kRSeg + lane * 8;
+        const float xp[8] = {pv[s][0].x, pv[s][0].y, pv[s][0].z, pv[s][0].w,
+                             pv[s][1].x, pv[s][1].y, pv[s][1].z, pv[s][1].w};
+        const float xq[8] = {qv[s][0].x, qv[s][0].y, qv[s][0].z, qv[s][0].w,
+                             qv[s][1].x, qv[s][1].y, qv[s][1].z, qv[s][1].w};
+        tot[s] = seg_sum(xp, xq, t0);
+      }
+    } else {
+      // rows not fit for bulk copies: nothing was staged, read them here
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar);
+      for (int s = 0; s < spw; ++s) {
+        const int t0 = (warp * spw + s) * kRSeg + lane * 8;
+        float xp[8], xq[8];
+        load8(mt.src, es, false, t0, mt.n_el, xp);
+        load8(mt.src2, es, false, t0, mode == 0 ? mt.n_el : 0, xq);
+        const float v = seg_sum(xp, xq, t0);
+        if (s == 0) tot[0] = v;
+        else if (s == 1) tot[1] = v;
+        else if (s == 2) tot[2] = v;
+        else tot[3] = v;
+      }
+    }
+    return make_float4(tot[0], tot[1], tot[2], tot[3]);
+  }
+
+  __device__ void store_segsums(const ResMeta& rm, int lane, float4 v) const {
+    const int spw = segs_per_chunk() / kGroupWarps;
+    if (lane < kGroupWarps) {
+      float* d = ws.segsums + rm.slot + lane * spw;
+      if (spw == 4) {
+        *reinterpret_cast<float4*>(d) = v;
+      } else {
+        d[0] = v.x;
+        if (spw > 1) d[1] = v.y;
+        if (spw > 2) d[2] = v.z;
+      }
+    }
+  }
+
+  __device__ float4 consume(const StageMeta& mt, const unsigned char* sp, uint64_t* empty_bar,
                             int ctid, int lane) const {
-    return reduce_row_chunk(mt, sp, empty_bar, ctid, lane, bulk, es);
+    if (mt.kind == KIND_RESID_PASS) return consume_resid(mt, sp, empty_bar, ctid, lane);
+    const float2 r = reduce_row_chunk(mt, sp, empty_bar, ctid, lane, bulk, es);
+    return make_float4(r.x, r.y, 0.f, 0.f);
   }
 
-  __device__ void finalize(Shared& sh, const PosTables& tab, int pos, int ftid) const;
+  __device__ void finalize_warp(Shared& sh, const PosTables& tab, int code, int lane,
+                                WarpFin& wf) const {
+    if (code & kFinResid) draw_finalize(code & ~kFinResid, lane, wf);
+    else request_finalize(sh, tab, code, lane, wf);
+  }
+  __device__ void request_finalize(Shared& sh, const PosTables& tab, int pos, int lane,
+                                   WarpFin& wf) const;
+  __device__ void draw_finalize(int b, int lane, WarpFin& wf) const;
   __device__ void last_cta_reset() const {}
 };
 
-// Residual / bonus weights of 32 consecutive tokens (tree walk helper).
-struct ChainWeights {
-  const char* prow;
-  const char* qrow;  // nullptr: bonus mode, w = 2^((l - m_p) c)
-  float mp, mq, izp, izq;
-  Scale2 c;
-  int es, V;
-  bool vec_ok;
-  __device__ void operator()(int i0, float* w) const {
-    float x[32];
-    load32(prow, es, vec_ok, i0, V, x);
-    if (qrow == nullptr) {
+// Merge the chunk partials of a request's rows into wf: lane j takes row j
+// (passes of 32 rows) and reads its ipr partials itself, eight loads in
+// flight at a time -- no shuffles, and one exp2 per partial, because the
+// consumers keep the shared-memory and special-function pipes of the SM
+// busy while finalizes run.  Softmax rows: the maximum first, then each
+// sum rescaled once to it; argmax rows: the largest value, lowest index.
+__device__ __forceinline__ void merge_rows(const float2* partials, int r0, int nrows, int ipr,
+                                           bool greedy, Scale2 c, int lane, WarpFin& wf) {
+  for (int j = lane; j < nrows; j += 32) {
+    const float2* pp = partials + static_cast<size_t>(r0 + j) * ipr;
+    float2 t[8];
+    if (greedy) {
+      VI v{kNegInf, 0x7fffffff};
+      for (int c0 = 0; c0 < ipr; c0 += 8) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) w[j] = fast_exp2(scaled_arg(x[j], mp, c));
-      return;
-    }
-    float y[32];
-    load32(qrow, es, vec_ok, i0, V, y);
+        for (int k = 0; k < 8; ++k)
+          t[k] = c0 + k < ipr ? __ldcg(pp + c0 + k)
+                              : make_float2(kNegInf, __int_as_float(0x7fffffff));
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float pv = fast_exp2(scaled_arg(x[j], mp, c)) * izp;
-      const float qv = fast_exp2(scaled_arg(y[j], mq, c)) * izq;
-      w[j] = fmaxf(pv - qv, 0.f);
+        for (int k = 0; k < 8; ++k) v = vi_better(v, VI{t[k].x, __float_as_int(t[k].y)});
+      }
+      wf.rm[j] = v.v;
+      wf.ridx[j] = v.i;
+    } else {
+      float M = kNegInf;
+      bool nan = false;
+      for (int c0 = 0; c0 < ipr; c0 += 8) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) t[k] = c0 + k < ipr ? __ldcg(pp + c0 + k) : make_float2(kNegInf, 0.f);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          nan |= t[k].x != t[k].x;
+          M = fmaxf(M, t[k].x);
+        }
+      }
+      float sum = 0.f;
+      if (!nan && M != kNegInf) {
+        for (int c0 = 0; c0 < ipr; c0 += 8) {
+          if (c0 > 0) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              t[k] = c0 + k < ipr ? __ldcg(pp + c0 + k) : make_float2(kNegInf, 0.f);
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            if (t[k].x != kNegInf) sum += t[k].y * fast_exp2(scaled_arg(t[k].x, M, c));
+        }
+      }
+      wf.rm[j] = nan ? nan_f() : M;
+      wf.rz[j] = nan ? 0.f : sum;
     }
   }
-};
+  __syncwarp();
+}
 
-__device__ void ChainProblem::finalize(Shared& sh, const PosTables& tab, int pos,
-                                       int ftid) const {
-  FinScratch& fs = sh.fin;
-  const int warp = ftid >> 5, lane = ftid & 31;
+__device__ void ChainProblem::request_finalize(Shared& sh, const PosTables& tab, int pos,
+                                               int lane, WarpFin& wf) const {
   const int info = tab.info[pos];
   const int b = info_req(info), kind = info_kind(info), nd = info_extra(info);
   const int r0 = tab.rstart[pos];
@@ -169,141 +370,261 @@ __device__ void ChainProblem::finalize(Shared& sh, const PosTables& tab, int pos
   const Scale2 c{tab.scale[pos].x, tab.scale[pos].y};
   const bool greedy = kind == KIND_ARGMAX;
 
-  // (1) merge the chunk partials of every row: a warp takes 32 / ipr rows
-  // per pass, one group of ipr lanes per row (all loads issued first), then
-  // a guarded shfl_down tree within each group
-  {
-    const int width = ipr <= 32 ? ipr : 32;
-    const int rpw = 32 / width;
-    const int g = lane / width, r = lane % width;
-    for (int j0 = warp * rpw; j0 < nrows; j0 += kFinWarps * rpw) {
-      const int j = j0 + g;
-      const bool own = g < rpw && j < nrows;
-      const float2* pp = ws.partials + static_cast<size_t>(r0 + (own ? j : 0)) * ipr;
-      if (greedy) {
-        VI v{kNegInf, 0x7fffffff};
-        if (own)
-          for (int ch = r; ch < ipr; ch += width) {
-            const float2 u = __ldcg(pp + ch);
-            v = vi_better(v, VI{u.x, __float_as_int(u.y)});
-          }
-        for (int o = 1; o < width; o <<= 1) {
-          const VI w{__shfl_down_sync(0xffffffffu, v.v, o), __shfl_down_sync(0xffffffffu, v.i, o)};
-          if (r + o < width) v = vi_better(v, w);
-        }
-        if (own && r == 0) {
-          fs.rm[j] = v.v;
-          fs.ridx[j] = v.i;
-        }
-      } else {
-        MS v{kNegInf, 0.f};
-        if (own)
-          for (int ch = r; ch < ipr; ch += width) {
-            const float2 u = __ldcg(pp + ch);
-            v = ms_combine(v, MS{u.x, u.y}, c);
-          }
-        for (int o = 1; o < width; o <<= 1) {
-          const MS w{__shfl_down_sync(0xffffffffu, v.m, o), __shfl_down_sync(0xffffffffu, v.s, o)};
-          if (r + o < width) v = ms_combine(v, w, c);
-        }
-        if (own && r == 0) {
-          fs.rm[j] = v.m;
-          fs.rz[j] = v.s;
-        }
-      }
-    }
+  // loads that do not depend on the merge go out first: the draft tokens,
+  // their uniforms and the logits they gather
+  const int x = lane < nd ? tokens[static_cast<size_t>(b) * K + lane] : 0;
+  const float ui = lane < nd ? uniforms[static_cast<size_t>(b) * (K + 1) + lane] : 0.f;
+  const bool x_ok = x >= 0 && x < V;
+  float lx = 0.f, dx = 0.f;
+  if (!greedy && lane < nd && x_ok) {
+    lx = load_logit(trow(b, lane), es, x);
+    dx = load_logit(drow(b, lane), es, x);
   }
-  named_sync(1, kFinThreads);
+  merge_rows(ws.partials, r0, nrows, ipr, greedy, c, lane, wf);
 
-  // (2) accept tests and the prefix-terminating scan (warp 0, lane i = draft i)
-  if (warp == 0) {
-    int err = 0;
-    bool acc = false;
-    // every row must be finite and carry mass
-    for (int j = lane; j < nrows; j += 32) {
-      if (fs.rm[j] != fs.rm[j]) err |= 0x02;
-      else if (fs.rm[j] == kNegInf || (!greedy && !(fs.rz[j] > 0.f))) err |= 0x04;
-    }
-    const double cd = static_cast<double>(c.hi) + static_cast<double>(c.lo);
-    if (lane < nd) {
-      const int x = tokens[static_cast<size_t>(b) * K + lane];
-      if (x < 0 || x >= V) {
-        err |= 0x01;
-      } else if (greedy) {
-        acc = x == fs.ridx[lane];
-        if (p_at) p_at[static_cast<size_t>(b) * K + lane] = acc ? 1.f : 0.f;
-        if (q_at) q_at[static_cast<size_t>(b) * K + lane] = __int_as_float(0x7fc00000);
-      } else {
-        const char* trow = target + (static_cast<int64_t>(b) * (K + 1) + lane) * t_stride;
-        const char* drow = draft + (static_cast<int64_t>(b) * K + lane) * d_stride;
-        const float lx = load_logit(trow, es, x), dx = load_logit(drow, es, x);
-        const int jt = lane, jd = nd + 1 + lane;
-        const double p = exp2(static_cast<double>(lx - fs.rm[jt]) * cd) /
-                         static_cast<double>(fs.rz[jt]);
-        const double q = exp2(static_cast<double>(dx - fs.rm[jd]) * cd) /
-                         static_cast<double>(fs.rz[jd]);
-        const double u = static_cast<double>(uniforms[static_cast<size_t>(b) * (K + 1) + lane]);
-        acc = u * q < p;
-        if (p_at) p_at[static_cast<size_t>(b) * K + lane] = static_cast<float>(p);
-        if (q_at) q_at[static_cast<size_t>(b) * K + lane] = static_cast<float>(q);
-      }
-    } else if (lane < K) {
-      if (p_at) p_at[static_cast<size_t>(b) * K + lane] = __int_as_float(0x7fc00000);
+  // accept tests (lane i = draft i) and the prefix-terminating scan
+  int err = 0;
+  for (int j = lane; j < nrows; j += 32) {
+    if (wf.rm[j] != wf.rm[j]) err |= 0x02;
+    else if (wf.rm[j] == kNegInf || (!greedy && !(wf.rz[j] > 0.f))) err |= 0x04;
+  }
+  bool acc = false;
+  const double cd = static_cast<double>(c.hi) + static_cast<double>(c.lo);
+  if (lane < nd) {
+    if (!x_ok) {
+      err |= 0x01;
+    } else if (greedy) {
+      acc = x == wf.ridx[lane];
+      if (p_at) p_at[static_cast<size_t>(b) * K + lane] = acc ? 1.f : 0.f;
       if (q_at) q_at[static_cast<size_t>(b) * K + lane] = __int_as_float(0x7fc00000);
-    }
-    for (int i = 32 + lane; i < K; i += 32) {  // K <= 32 keeps this empty
-      if (p_at) p_at[static_cast<size_t>(b) * K + i] = __int_as_float(0x7fc00000);
-      if (q_at) q_at[static_cast<size_t>(b) * K + i] = __int_as_float(0x7fc00000);
-    }
-    err = __reduce_or_sync(0xffffffffu, err);
-    const unsigned mask = __ballot_sync(0xffffffffu, acc);
-    int n = mask == 0xffffffffu ? 32 : __ffs(~mask) - 1;
-    n = min(n, nd);
-    if (lane == 0) {
-      fs.n_acc = n;
-      fs.err = err;
+    } else {
+      const int jt = lane, jd = nd + 1 + lane;
+      // p(x) = np / Zp, q(x) = nq / Zq with np, nq in fp64; the test
+      // u q(x) < p(x) is taken as u nq Zp < np Zq (no division)
+      const double np = exp2_nonpos(
+          (static_cast<double>(lx) - static_cast<double>(wf.rm[jt])) * cd);
+      const double nq = exp2_nonpos(
+          (static_cast<double>(dx) - static_cast<double>(wf.rm[jd])) * cd);
+      const double zp = static_cast<double>(wf.rz[jt]), zq = static_cast<double>(wf.rz[jd]);
+      acc = static_cast<double>(ui) * nq * zp < np * zq;
+      // Z >= 1 (the maximum's own term), so the reciprocal needs no special cases
+      if (p_at) p_at[static_cast<size_t>(b) * K + lane] = static_cast<float>(np) * rcp_fma(wf.rz[jt]);
+      if (q_at) q_at[static_cast<size_t>(b) * K + lane] = static_cast<float>(nq) * rcp_fma(wf.rz[jd]);
     }
   }
-  named_sync(1, kFinThreads);
-  const int n = fs.n_acc;
-  const int err = fs.err;
-
-  // (3) the emitted token: greedy here; sampled requests hand the draw to
-  // the residual pass (one job: row pair n, residual or bonus)
-  int token = -1;
-  const int err2 = err;
-  if (!err && greedy) token = fs.ridx[n];
-  if (!err && !greedy && ftid == 0) {
-    const int jid = atomicAdd(&ws.hdr->n_jobs, 1);
-    ResidJob jb;
-    jb.b = b;
-    jb.n = n;
-    jb.mode = n < nd ? 0 : 1;
-    jb.mp = fs.rm[n];
-    jb.izp = 1.f / fs.rz[n];
-    jb.mq = n < nd ? fs.rm[nd + 1 + n] : 0.f;
-    jb.izq = n < nd ? 1.f / fs.rz[nd + 1 + n] : 0.f;
-    jb.c_hi = c.hi;
-    jb.c_lo = c.lo;
-    jobs[jid] = jb;
+  for (int i = max(lane, nd); i < K; i += 32) {
+    if (p_at) p_at[static_cast<size_t>(b) * K + i] = __int_as_float(0x7fc00000);
+    if (q_at) q_at[static_cast<size_t>(b) * K + i] = __int_as_float(0x7fc00000);
   }
+  err = __reduce_or_sync(0xffffffffu, err);
+  const unsigned mask = __ballot_sync(0xffffffffu, acc);
+  int n = mask == 0xffffffffu ? 32 : __ffs(~mask) - 1;
+  n = min(n, nd);
 
-  // (4) outputs; reset this request's ticket for the next call
-  if (ftid <= K) {
+  // outputs: the accepted prefix; greedy also the emitted token
+  for (int i = lane; i <= K; i += 32) {
     int v = -1;
-    if (!err2) {
-      if (ftid < n) v = tokens[static_cast<size_t>(b) * K + ftid];
-      else if (ftid == n) v = token;  // sampled: written by the residual pass
+    if (!err) {
+      if (i < n) v = tokens[static_cast<size_t>(b) * K + i];
+      else if (i == n && greedy) v = wf.ridx[n];
     }
-    out_tokens[static_cast<size_t>(b) * (K + 1) + ftid] = v;
+    out_tokens[static_cast<size_t>(b) * (K + 1) + i] = v;
   }
-  if (ftid == 0) {
-    out_len[b] = err2 ? 0 : n + 1;
-    accept_len[b] = err2 ? 0 : n;
-    if (err2) record_error(&ws.hdr->error, err2);
-    ws.tickets[b] = 0u;
+  __syncwarp();  // every lane's outputs before lane 0's release below
+  if (lane == 0) {
+    out_len[b] = err ? 0 : n + 1;
+    accept_len[b] = err ? 0 : n;
+    if (err) record_error(&ws.hdr->error, err);
+    ws.tickets[b] = 0u;  // ready for the next call
+    if (!err && !greedy) {
+      // the draw from norm(max(0, p_n - q_n)) (rejection) or p_nd (bonus)
+      P2Job jb;
+      jb.b = b;
+      jb.n = n;
+      jb.mode = n < nd ? 0 : 1;
+      jb.mp = wf.rm[n];
+      jb.izp = 1.f / wf.rz[n];
+      jb.mq = n < nd ? wf.rm[nd + 1 + n] : 0.f;
+      jb.izq = n < nd ? 1.f / wf.rz[nd + 1 + n] : 0.f;
+      jb.c_hi = c.hi;
+      jb.c_lo = c.lo;
+      jb.pad[0] = jb.pad[1] = jb.pad[2] = 0;
+      jobs[b] = jb;
+      const unsigned d = atomicAdd(&ws.hdr->draw_reserve, 1u);
+      st_release(ws.draws + d, b + 1);  // the job (and the outputs) before the entry
+    }
+    atomic_add_release(&ws.hdr->fin_count, 1u);  // the draw list entry before the count
   }
-  named_sync(1, kFinThreads);
+  __syncwarp();
+}
+
+// Lane l's 16 segment sums of page g (segments [512 g + 16 l, +16)), zero
+// beyond nseg (a multiple of 4).
+__device__ __forceinline__ void load_page(const float* ss, int nseg, int g, int lane, float* v) {
+  const int i0 = g * kPageSeg + lane * 16;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i0 + 4 * q < nseg) f = __ldcg(reinterpret_cast<const float4*>(ss + i0 + 4 * q));
+    v[4 * q] = f.x;
+    v[4 * q + 1] = f.y;
+    v[4 * q + 2] = f.z;
+    v[4 * q + 3] = f.w;
+  }
+}
+
+// The draw from the weights of the draw pass: S = the sum of the segment
+// sums, target = u_K S, the segment whose running sum first exceeds target
+// (pages of 512 segments, then the lane's block of 16, then the segment),
+// then the token within it.  Running sums are float pairs; the search goes
+// in ascending token order throughout, as the inverse CDF does.
+__device__ void ChainProblem::draw_finalize(int b, int lane, WarpFin& wf) const {
+  const P2Job jb = load_job(b);
+  const int n = jb.n, mode = jb.mode;
+  const int nseg = ipr2 * segs_per_chunk();
+  float* ss = ws.segsums + static_cast<size_t>(b) * nseg;
+  const float u = uniforms[static_cast<size_t>(b) * (K + 1) + K];
+  const char* pr = trow(b, n);
+  const char* qr = mode == 0 ? drow(b, n) : nullptr;
+  ResidParams rp{jb.mp, jb.izp, jb.mq, jb.izq, Scale2{jb.c_hi, jb.c_lo}, mode};
+  const int npages = (nseg + kPageSeg - 1) / kPageSeg;
+  int token = -1;
+  for (int attempt = 0; attempt < 2 && token < 0; ++attempt) {
+    if (attempt == 1) {
+      if (mode != 0) break;
+      // a residual of zero mass (rounding only): draw from p_n instead --
+      // recompute the segment sums with the bonus weights
+      rp.mode = 1;
+      qr = nullptr;
+      for (int k = 0; k < nseg; ++k) {
+        const int t0 = k * kRSeg + lane * 8;
+        float xp[8], xq[8], w[8];
+        load8(pr, es, bulk, t0, V, xp);
+        load8(pr, es, bulk, t0, 0, xq);
+        const float ls = resid_weights8(xp, xq, t0, V, rp, w);
+        const float inc = warp_incl_scan_rn(ls, lane);
+        if (lane == 31) __stcg(ss + k, inc);
+      }
+      __threadfence_block();
+      __syncwarp();
+    }
+    // page totals (kept in the warp's scratch) and S
+    float v[16];
+    DF S{0.f, 0.f};
+    for (int g = 0; g < npages; ++g) {
+      load_page(ss, nseg, g, lane, v);
+      DF bs{0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < 16; ++j) bs = df_add(bs, v[j]);
+      const DF tot = df_shfl(warp_incl_scan_df(bs, lane), 31);
+      if (lane == 0) {
+        wf.rz[2 * g] = tot.hi;
+        wf.rz[2 * g + 1] = tot.lo;
+      }
+      S = df_add(S, tot);
+    }
+    __syncwarp();
+    if (!(S.hi > 0.f)) continue;
+    const DF target = df_mul(u, S);
+    // the page holding target (target < S, so there is one)
+    int pg = -1;
+    DF base{0.f, 0.f}, run{0.f, 0.f};
+    for (int g = 0; g < npages; ++g) {
+      const DF nxt = df_add(run, DF{wf.rz[2 * g], wf.rz[2 * g + 1]});
+      if (pg < 0 && df_lt(target, nxt)) {
+        pg = g;
+        base = run;
+      }
+      run = nxt;
+    }
+    if (pg < 0) continue;
+    if (pg != npages - 1) load_page(ss, nseg, pg, lane, v);
+    // the lane whose block holds target
+    DF bs{0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 16; ++j) bs = df_add(bs, v[j]);
+    const DF incl = warp_incl_scan_df(bs, lane);
+    const unsigned hit = __ballot_sync(0xffffffffu, df_lt(target, df_add(base, incl)));
+    if (!hit) continue;
+    const int owner = __ffs(hit) - 1;
+    const DF prev = df_shfl(incl, owner > 0 ? owner - 1 : 0);
+    const DF lane_base = owner > 0 ? df_add(base, prev) : base;
+    // the segment within the owner's block
+    int k = -1;
+    DF seg_base = lane_base;
+    if (lane == owner) {
+      DF r = lane_base;
+      int lastp = -1;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const DF nx = df_add(r, v[j]);
+        if (k < 0 && df_lt(target, nx)) {
+          k = j;
+          seg_base = r;
+        }
+        if (v[j] > 0.f) lastp = j;
+        r = nx;
+      }
+      if (k < 0) {
+        k = lastp;  // rounding: the last segment of the block with mass
+        seg_base.hi = -1.f;
+      }
+      if (k >= 0) k += pg * kPageSeg + owner * 16;
+    }
+    k = __shfl_sync(0xffffffffu, k, owner);
+    seg_base = df_shfl(seg_base, owner);
+    if (k < 0) continue;
+    const bool in_seg = seg_base.hi >= 0.f;
+    // rescan segment k exactly as the draw pass computed it
+    const int t0 = k * kRSeg + lane * 8;
+    float xp[8], xq[8], w[8];
+    load8(pr, es, bulk, t0, V, xp);
+    load8(qr, es, bulk, t0, qr ? V : 0, xq);
+    const float ls = resid_weights8(xp, xq, t0, V, rp, w);
+    const float inc = warp_incl_scan_rn(ls, lane);
+    float exl = __shfl_up_sync(0xffffffffu, inc, 1);
+    if (lane == 0) exl = 0.f;
+    int tok = -1, src;
+    int lastp = -1;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (w[j] > 0.f) lastp = j;
+    if (in_seg) {
+      const unsigned lh = __ballot_sync(0xffffffffu, df_lt(target, df_add(seg_base, inc)));
+      src = lh ? __ffs(lh) - 1 : 31;
+      DF cc = df_add(seg_base, exl);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        cc = df_add(cc, w[j]);
+        if (tok < 0 && df_lt(target, cc)) tok = j;
+      }
+      if (tok < 0) tok = lastp;
+      if (!lh) {
+        // rounding left target beyond the segment: its last positive weight
+        const unsigned lp = __ballot_sync(0xffffffffu, lastp >= 0);
+        src = lp ? 31 - __clz(lp) : 31;
+        tok = lastp;
+      }
+    } else {
+      const unsigned lp = __ballot_sync(0xffffffffu, lastp >= 0);
+      src = lp ? 31 - __clz(lp) : 0;
+      tok = lastp;
+    }
+    tok = __shfl_sync(0xffffffffu, tok, src);
+    token = tok < 0 ? -1 : k * kRSeg + src * 8 + tok;
+  }
+  if (lane == 0) {
+    if (token >= 0) {
+      out_tokens[static_cast<size_t>(b) * (K + 1) + n] = token;
+    } else {
+      for (int i = 0; i <= K; ++i) out_tokens[static_cast<size_t>(b) * (K + 1) + i] = -1;
+      out_len[b] = 0;
+      accept_len[b] = 0;
+      record_error(&ws.hdr->error, 0x04);
+    }
+    ws.tickets[kDrawTicketBase + b] = 0u;
+  }
+  __syncwarp();
 }
 
 }  // namespace sv

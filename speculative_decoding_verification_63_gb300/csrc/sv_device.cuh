@@ -121,6 +121,55 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// 2^x in fp64 for x <= 0 (x = -inf gives 0).  x = n + f with n = rint(x)
+// and |f| <= 1/2; 2^f = e^t, t = f ln 2, |t| < 0.347, by the Taylor series
+// of e^t to degree 13 (truncation below 4e-18 relative) in Horner form;
+// 2^n is applied through the exponent field in two factors so that results
+// down to the subnormal range come out right.  About 20 fp64 operations:
+// much shorter than a general-purpose exp2 on a part whose fp64 rate is low.
+__device__ __forceinline__ double exp2_nonpos(double x) {
+  if (!(x > -1080.0)) return 0.0;
+  const double n = rint(x);
+  const double t = (x - n) * 0.69314718055994530942;
+  // 1/k!, evaluated at compile time
+  constexpr double f2 = 1.0 / 2, f3 = f2 / 3, f4 = f3 / 4, f5 = f4 / 5, f6 = f5 / 6;
+  constexpr double f7 = f6 / 7, f8 = f7 / 8, f9 = f8 / 9, f10 = f9 / 10, f11 = f10 / 11;
+  constexpr double f12 = f11 / 12, f13 = f12 / 13;
+  double e = fma(f13, t, f12);
+  e = fma(e, t, f11);
+  e = fma(e, t, f10);
+  e = fma(e, t, f9);
+  e = fma(e, t, f8);
+  e = fma(e, t, f7);
+  e = fma(e, t, f6);
+  e = fma(e, t, f5);
+  e = fma(e, t, f4);
+  e = fma(e, t, f3);
+  e = fma(e, t, f2);
+  e = fma(e, t, 1.0);
+  e = fma(e, t, 1.0);
+  const int ni = static_cast<int>(n);  // -1080 .. 0
+  const int n1 = ni / 2, n2 = ni - n1;
+  const double s1 = __longlong_as_double(static_cast<long long>(1023 + n1) << 52);
+  const double s2 = __longlong_as_double(static_cast<long long>(1023 + n2) << 52);
+  return (e * s1) * s2;
+}
+
+// 1/z for 2^-125 <= z <= 2^125 with fused multiply-adds only (no special-
+// function unit, which the streaming reduction keeps busy): z = m 2^e with
+// m in [1/2, 1), the linear start 48/17 - 32/17 m (relative error at most
+// 1/17), three Newton-Raphson steps y += y (1 - m y) (error squared each
+// step), then the exponent.  Accurate to about one ulp.
+__device__ __forceinline__ float rcp_fma(float z) {
+  const unsigned zb = __float_as_uint(z);
+  const int e = static_cast<int>((zb >> 23) & 0xffu) - 126;
+  const float m = __uint_as_float((zb & 0x007fffffu) | 0x3f000000u);
+  float y = __fmaf_rn(-32.f / 17.f, m, 48.f / 17.f);
+#pragma unroll
+  for (int k = 0; k < 3; ++k) y = __fmaf_rn(y, __fmaf_rn(-m, y, 1.f), y);
+  return __uint_as_float(__float_as_uint(y) - (static_cast<unsigned>(e) << 23));
+}
+
 // Packed max of two bf16 pairs, NaN-propagating.
 __device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
   uint32_t r;
@@ -216,6 +265,65 @@ __device__ __forceinline__ double warp_incl_scan_d(double x, int lane) {
   return x;
 }
 
+// ------------------------------------------------- float-pair (hi + lo) sums
+
+// An unevaluated pair hi + lo for running sums that must stay far more
+// accurate than fp32 rounding (about 2^-44 relative) without fp64, which is
+// slow on this part.  Built on the error-free sum of two floats (Knuth's
+// TwoSum) and on the fused multiply-add residual of a product; every step
+// is an explicitly rounded intrinsic so the compiler cannot contract it.
+struct DF {
+  float hi, lo;
+};
+
+__device__ __forceinline__ DF two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bp = __fsub_rn(s, a);
+  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+  return DF{s, e};
+}
+
+// (a + b) renormalised, for |a| >= |b| or a == 0
+__device__ __forceinline__ DF quick_two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  return DF{s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+
+__device__ __forceinline__ DF df_add(DF x, float y) {
+  const DF s = two_sum(x.hi, y);
+  return quick_two_sum(s.hi, __fadd_rn(s.lo, x.lo));
+}
+
+__device__ __forceinline__ DF df_add(DF x, DF y) {
+  const DF s = two_sum(x.hi, y.hi);
+  return quick_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(x.lo, y.lo)));
+}
+
+// u * x for a float u
+__device__ __forceinline__ DF df_mul(float u, DF x) {
+  const float p = __fmul_rn(u, x.hi);
+  const float e = __fmaf_rn(u, x.hi, -p);
+  return quick_two_sum(p, __fmaf_rn(u, x.lo, e));
+}
+
+__device__ __forceinline__ bool df_lt(DF a, DF b) {
+  return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo);
+}
+
+__device__ __forceinline__ DF df_shfl(DF x, int src) {
+  return DF{__shfl_sync(0xffffffffu, x.hi, src), __shfl_sync(0xffffffffu, x.lo, src)};
+}
+
+// Inclusive warp scan of pairs (Kogge-Stone).
+__device__ __forceinline__ DF warp_incl_scan_df(DF x, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const DF y{__shfl_up_sync(0xffffffffu, x.hi, o), __shfl_up_sync(0xffffffffu, x.lo, o)};
+    if (lane >= o) x = df_add(y, x);
+  }
+  return x;
+}
+
 __device__ __forceinline__ void record_error(int* err, int flag) { atomicOr(err, flag); }
 
 // Fetch-and-add with acquire-release semantics at GPU scope: orders this
@@ -227,6 +335,37 @@ __device__ __forceinline__ unsigned atomic_add_acq_rel(unsigned* p, unsigned v) 
   asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
                : "memory");
   return old;
+}
+
+// Loads and stores with GPU-scope ordering, for flags that other CTAs read.
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned ld_relaxed(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_relaxed(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+__device__ __forceinline__ void st_release(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void atomic_add_release(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 }  // namespace sv

@@ -1,35 +1,65 @@
 // sv_kernel.cuh -- the persistent verification kernel, generic over the
 // problem (chain or tree).
 //
-// One CTA per SM, four warp roles:
-//   warps 0..15  consumers: each warp reduces its sixteenth of every staged
-//                chunk, releases the stage as soon as the data is in
-//                registers, and posts its partial into the result ring.
-//   warp  16     producer: claims chunks with a global atomic counter and
-//                moves them into the 4-stage ring with 1-D bulk copies.
-//   warp  17     bookkeeper: takes result slots in order, combines the 16
+// One CTA per SM, five warp roles (control warps first, so that the warp
+// schedulers, which favour lower warp ids, serve them ahead of the
+// always-ready consumers):
+//   warp  0      producer: moves chunks into the 4-stage ring with 1-D bulk
+//                copies: first the CTA's share of the main pass (chunks
+//                blockIdx.x, blockIdx.x + gridDim.x, ...), then draw-pass
+//                chunks claimed from a global counter; claim g is chunk
+//                g % ipr2 of the (g / ipr2)-th draw that request finalizes
+//                published in the global draw list (a claim waits for its
+//                draw, or lapses once every request is finalized and the
+//                list ends before it).  The 32 lanes work out the main-pass
+//                chunks 32 at a time (one each) and copy each chunk's
+//                metadata into the ring together; lane 0 waits for the slots
+//                and issues the copies.  With nothing left the producer ends
+//                the stream with one sentinel per consumer group.
+//   warp  1      bookkeeper: takes result slots in order, combines the 8
 //                per-warp partials of a chunk (max first, one rescale, a
-//                sum), stores one partial per chunk and bumps the per-request
-//                tickets in lane-parallel batches; a request whose last
-//                chunk is in joins the finalize list.
-//   warps 18..21 finalizer group: runs each listed request's finalize while
-//                the consumers keep streaming.
-// Every hand-off is an mbarrier (or, for the finalize list, a counter polled
-// with back-off); all waits are bounded.
+//                sum) or keeps the residual segment sums, stores them and
+//                appends the chunk's ticket to the booked queue.
+//   warp  2      ticket warp: takes booked chunks in lane-parallel batches,
+//                fences, bumps the tickets; a completed request or residual
+//                draw joins the finalize list.
+//   warps 3..6   finalizers: take finalize-list entries (each warp on its
+//                own, or the four together for problems that need a group)
+//                while the consumers keep streaming.
+//   warps 7..22  consumers, in two groups of eight that take alternate
+//                chunks (so each group has two chunk times per chunk): each
+//                warp reduces its eighth of the chunk, releases the stage as
+//                soon as the data is in registers, and posts its partial
+//                into the result ring.
+// Every hand-off is an mbarrier or a shared counter polled with back-off;
+// every wait is bounded.  The one wait on other CTAs -- a draw-pass claim
+// waiting for its draw -- only ever waits on CTAs that are running: the
+// grid never exceeds the SM count and a CTA holds the whole of an SM, and
+// a draw depends only on main-pass chunks and on finalizes, which never
+// wait on other CTAs.
 //
 // A problem type P provides:
 //   int n_req, ipr, chunk_el, es, V; bool bulk; Ws ws;
-//   static constexpr int kAuxBytes  (per-position aux table, 0, 8 or 16)
-//   void preamble(Shared&, PosTables&, int4* scan_tmp) const  (all threads)
-//   void fill_stage(const PosTables&, int row_local, StageMeta&) const
-//        -> kind, scale, source pointer(s) and aux of a chunk (producer)
-//   float2 consume(const StageMeta&, const unsigned char* stage,
+//   static constexpr int kAuxBytes       per-position aux table (0, 8, 16)
+//   static constexpr bool kWarpFinalize  finalizes run per warp (else group)
+//   static constexpr bool kHasDraws      the problem publishes draw passes
+//   void preamble(Shared&, PosTables&, int4* scan_tmp) const   (all threads)
+//   void fill_stage(const PosTables&, int row_local, StageMeta&, ResMeta&)
+//        -> a main-pass chunk: kind, scale, source, ticket fields (producer)
+//   void fill_resid(const P2Job&, int chunk, StageMeta&, ResMeta&) const
+//        -> a draw-pass chunk (producer)
+//   int ipr2                     chunks per draw
+//   P2Job load_job(int b) const  the draw published for request b
+//   void store_segsums(const ResMeta&, int lane, float4) const
+//        -> the bookkeeper's store of a draw-pass chunk's segment sums
+//   float4 consume(const StageMeta&, const unsigned char* stage,
 //                  uint64_t* empty_bar, int ctid, int lane) const
-//        -> the warp's partial of a chunk; arrives on empty_bar once the
-//           staged data is no longer needed (consumer warps)
-//   void finalize(Shared&, const PosTables&, int pos, int ftid) const
-//        (called by the kFinThreads finalizer threads)
-//   void last_cta_reset() const   (the last CTA to finish, after every other)
+//        (ctid: thread index within the consumer group)
+//   void finalize_warp(Shared&, const PosTables&, int code, int lane,
+//                      WarpFin&) const     (kWarpFinalize)
+//   void finalize(Shared&, const PosTables&, int code, int ftid) const
+//                                          (!kWarpFinalize, all 4 warps)
+//   void last_cta_reset() const  (the last CTA to finish, after all others)
 #pragma once
 
 #include "sv_rowpass.cuh"
@@ -66,69 +96,222 @@ __device__ __forceinline__ void wait_or_flag(Shared& sh, uint64_t* bar, uint32_t
   }
 }
 
+__device__ __forceinline__ unsigned vload(const unsigned& x) {
+  return *reinterpret_cast<const volatile unsigned*>(&x);
+}
+
+// Give up a bounded wait: flag the timeout (later waits of this CTA are short).
+__device__ __forceinline__ void flag_timeout(Shared& sh, int* err) {
+  sh.timed_out = 1;
+  record_error(err, 0x10);
+}
+
 template <class P>
 __device__ void producer_loop(const P& prob, Shared& sh, const PosTables& tab,
                               unsigned char* stages) {
-  int* err = &prob.ws.hdr->error;
+  WsHeader* hdr = prob.ws.hdr;
+  int* err = &hdr->error;
+  const int lane = threadIdx.x & 31;
   const int n_pos = sh.n_pos;
   const int n_rows = tab.rstart[n_pos];
   const unsigned n_items = static_cast<unsigned>(n_rows) * static_cast<unsigned>(prob.ipr);
-  unsigned item = atomicAdd(&prob.ws.hdr->work_counter, 1u);
-  int hint = 0;
-  for (int it = 0;; ++it) {
+  const unsigned G = gridDim.x;
+  int it = 0;                 // ring position
+
+  // Issue plan record k into the ring (all lanes): lane 0 waits for the
+  // slot, the lanes copy the record word by word, lane 0 publishes it and
+  // starts the bulk copies.
+  auto issue = [&](int k) {
     const int stage = it % kStages;
     const int rs = it % kResSlots;
-    const bool have = item < n_items;
-    const unsigned next = have ? atomicAdd(&prob.ws.hdr->work_counter, 1u) : 0u;
-    if (it >= kStages) wait_or_flag(sh, &sh.empty[stage], ((it / kStages) - 1) & 1, err);
-    if (it >= kResSlots) wait_or_flag(sh, &sh.res_free[rs], ((it / kResSlots) - 1) & 1, err);
-    StageMeta& mt = sh.meta[stage];
-    ResMeta& rm = sh.res_meta[rs];
-    if (!have) {
+    if (lane == 0) {
+      if (it >= kStages) wait_or_flag(sh, &sh.empty[stage], ((it / kStages) - 1) & 1, err);
+      if (it >= kResSlots) wait_or_flag(sh, &sh.res_free[rs], ((it / kResSlots) - 1) & 1, err);
+    }
+    __syncwarp();
+    if (lane < kMetaWords)
+      reinterpret_cast<int*>(&sh.meta[stage])[lane] = reinterpret_cast<const int*>(&sh.plan_m[k])[lane];
+    else if (lane < kMetaWords + kResWords)
+      reinterpret_cast<int*>(&sh.res_meta[rs])[lane - kMetaWords] =
+          reinterpret_cast<const int*>(&sh.plan_r[k])[lane - kMetaWords];
+    __syncwarp();  // every lane's words before lane 0's arrivals
+    if (lane == 0) {
+      const StageMeta& m = sh.plan_m[k];
+      mbar_arrive(&sh.res_done[rs]);
+      if (prob.bulk) {
+        // one or two row pieces of n_el elements: [0, half) and [half, 2 half)
+        const uint32_t bytes = static_cast<uint32_t>(m.n_el * prob.es);
+        const char* src2 = m.src2;
+        unsigned char* dst = stages + static_cast<size_t>(stage) * kChunkBytes;
+        mbar_arrive_expect_tx(&sh.full[stage], src2 ? 2u * bytes : bytes);
+        bulk_copy_g2s(dst, m.src, bytes, &sh.full[stage]);
+        if (src2) bulk_copy_g2s(dst + kChunkBytes / 2, src2, bytes, &sh.full[stage]);
+      } else {
+        mbar_arrive(&sh.full[stage]);
+      }
+    }
+    __syncwarp();
+    ++it;
+  };
+
+  // Draw-pass claims run alongside the main pass (lane 0): a claim is taken
+  // when the CTA starts; once per issued main-pass chunk the claim machine
+  // advances one step (read the claim, poll the draw list, fetch the job,
+  // plan the chunk); a planned draw chunk goes into the ring ahead of the
+  // next main-pass chunk and the next claim is taken.  Claim g is chunk
+  // g % ipr2 of the (g / ipr2)-th published draw; claims beyond the number
+  // of sampled requests lapse at once.
+  enum { D_NONE, D_CLAIMED, D_POLL, D_JOB };
+  int dstate = D_NONE;
+  unsigned dclaim = 0;
+  int poll = 0;
+  P2Job job{};
+  const unsigned cap = P::kHasDraws ? static_cast<unsigned>(sh.n_draw_cap) : 0u;
+  if (lane == 0 && cap > 0) {
+    dclaim = atomicAdd(&hdr->work_counter, 1u);
+    dstate = D_CLAIMED;
+  }
+  auto draw_step = [&]() -> bool {
+    if constexpr (P::kHasDraws) {
+      const unsigned d = dclaim / static_cast<unsigned>(prob.ipr2);
+      if (dstate == D_CLAIMED) {
+        if (d >= cap) {
+          dstate = D_NONE;
+          return false;
+        }
+        poll = ld_relaxed(prob.ws.draws + d);
+        dstate = D_POLL;
+      } else if (dstate == D_POLL) {
+        if (poll > 0) {
+          fence_acq_rel_gpu();  // the job, published before the entry
+          job = prob.load_job(poll - 1);
+          dstate = D_JOB;
+        } else {
+          poll = ld_relaxed(prob.ws.draws + d);
+        }
+      } else if (dstate == D_JOB) {
+        StageMeta& mt = sh.plan_m[kDrawSlot];
+        ResMeta& rm = sh.plan_r[kDrawSlot];
+        mt.item = 0x7fffffff;
+        mt.pos = -1;
+        mt.src2 = nullptr;
+        prob.fill_resid(job, static_cast<int>(dclaim % static_cast<unsigned>(prob.ipr2)), mt, rm);
+        rm.item = mt.item;
+        rm.kind = mt.kind;
+        rm.c_hi = mt.c_hi;
+        rm.c_lo = mt.c_lo;
+        dclaim = atomicAdd(&hdr->work_counter, 1u);
+        dstate = D_CLAIMED;
+        return true;
+      }
+    }
+    return false;
+  };
+
+  // Main pass: this CTA's share (chunks blockIdx.x + j G), worked out 32 at
+  // a time, one chunk per lane, then issued in order.
+  for (unsigned base = blockIdx.x; base < n_items; base += 32u * G) {
+    const int cnt = static_cast<int>(min(32u, (n_items - base + G - 1u) / G));
+    if (lane < cnt) {
+      const unsigned item = base + static_cast<unsigned>(lane) * G;
+      StageMeta& mt = sh.plan_m[lane];
+      ResMeta& rm = sh.plan_r[lane];
+      const int row = static_cast<int>(item / prob.ipr);
+      const int chunk = static_cast<int>(item % prob.ipr);
+      const int pos = find_pos(tab.rstart, n_pos, row, -1);
+      mt.item = static_cast<int>(item);
+      mt.pos = pos;
+      mt.el_base = chunk * prob.chunk_el;
+      mt.n_el = min(prob.chunk_el, prob.V - mt.el_base);
+      mt.src2 = nullptr;
+      rm.slot = row * prob.ipr + chunk;
+      prob.fill_stage(tab, row - tab.rstart[pos], mt, rm);
+      rm.item = mt.item;
+      rm.kind = mt.kind;
+      rm.c_hi = mt.c_hi;
+      rm.c_lo = mt.c_lo;
+    }
+    __syncwarp();
+    for (int k = 0; k < cnt; ++k) {
+      int have_draw = 0;
+      if (lane == 0 && dstate != D_NONE) have_draw = draw_step() ? 1 : 0;
+      if (__shfl_sync(0xffffffffu, have_draw, 0)) issue(kDrawSlot);
+      issue(k);
+    }
+  }
+
+  if constexpr (P::kHasDraws) {
+    // The rest of the draw pass: lane 0 runs the claim machine until a chunk
+    // is planned, or the claim lapses (beyond the sampled requests, or every
+    // request finalized and the list shorter than its draw).
+    for (;;) {
+      int have = 0;
+      if (lane == 0) {
+        uint64_t t0 = 0;
+        unsigned backoff = 64;
+        while (dstate != D_NONE) {
+          if (draw_step()) {
+            have = 1;
+            break;
+          }
+          if (dstate == D_POLL && poll <= 0) {
+            const unsigned d = dclaim / static_cast<unsigned>(prob.ipr2);
+            if (ld_acquire(&hdr->fin_count) == static_cast<unsigned>(prob.n_req) &&
+                ld_relaxed(&hdr->draw_reserve) <= d) {
+              dstate = D_NONE;  // the list is final and ends before d
+              break;
+            }
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) t0 = now;
+            if (now - t0 > wait_limit(sh)) {
+              flag_timeout(sh, err);
+              dstate = D_NONE;
+              break;
+            }
+            __nanosleep(backoff);
+            backoff = min(backoff * 2u, 512u);
+          }
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, have, 0)) break;
+      issue(kDrawSlot);
+    }
+  }
+
+  // end of stream: one sentinel per consumer group (the bookkeeper stops at
+  // the first)
+  for (int k = 0; k < kGroups; ++k) {
+    if (lane == 0) {
+      StageMeta& mt = sh.plan_m[0];
+      ResMeta& rm = sh.plan_r[0];
       mt.item = -1;
+      mt.n_el = 0;
+      mt.src2 = nullptr;
       rm.item = -1;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      const int stage = it % kStages;
+      const int rs = it % kResSlots;
+      if (it >= kStages) wait_or_flag(sh, &sh.empty[stage], ((it / kStages) - 1) & 1, err);
+      if (it >= kResSlots) wait_or_flag(sh, &sh.res_free[rs], ((it / kResSlots) - 1) & 1, err);
+      sh.meta[stage].item = -1;
+      sh.res_meta[rs].item = -1;
       mbar_arrive(&sh.res_done[rs]);
       mbar_arrive(&sh.full[stage]);
-      break;
     }
-    const int row = static_cast<int>(item / prob.ipr);
-    const int chunk = static_cast<int>(item % prob.ipr);
-    const int pos = find_pos(tab.rstart, n_pos, row, hint);
-    hint = pos;
-    mt.item = static_cast<int>(item);
-    mt.pos = pos;
-    mt.row = row;
-    mt.el_base = chunk * prob.chunk_el;
-    mt.n_el = min(prob.chunk_el, prob.V - mt.el_base);
-    mt.src2 = nullptr;
-    prob.fill_stage(tab, row - tab.rstart[pos], mt);
-    rm.item = static_cast<int>(item);
-    rm.pos = pos;
-    rm.slot = row * prob.ipr + chunk;
-    rm.kind = mt.kind;
-    rm.c_hi = mt.c_hi;
-    rm.c_lo = mt.c_lo;
-    mbar_arrive(&sh.res_done[rs]);
-    if (prob.bulk) {
-      // one or two row pieces of n_el elements: [0, half) and [half, 2 half)
-      const uint32_t bytes = static_cast<uint32_t>(mt.n_el * prob.es);
-      unsigned char* dst = stages + static_cast<size_t>(stage) * kChunkBytes;
-      mbar_arrive_expect_tx(&sh.full[stage], mt.src2 ? 2u * bytes : bytes);
-      bulk_copy_g2s(dst, mt.src, bytes, &sh.full[stage]);
-      if (mt.src2) bulk_copy_g2s(dst + kChunkBytes / 2, mt.src2, bytes, &sh.full[stage]);
-    } else {
-      mbar_arrive(&sh.full[stage]);
-    }
-    item = next;
+    __syncwarp();
+    ++it;
   }
 }
 
 template <class P>
 __device__ void consumer_loop(const P& prob, Shared& sh, unsigned char* stages) {
   int* err = &prob.ws.hdr->error;
-  const int ctid = threadIdx.x;  // 0 .. kConsumers-1
+  const int group = (threadIdx.x - kConsBase) / kGroupThreads;
+  const int ctid = (threadIdx.x - kConsBase) % kGroupThreads;  // 0 .. kGroupThreads-1
   const int warp = ctid >> 5, lane = ctid & 31;
-  for (int j = 0;; ++j) {
+  for (int j = group;; j += kGroups) {
     const int stage = j % kStages;
     const int rs = j % kResSlots;
     wait_or_flag(sh, &sh.full[stage], (j / kStages) & 1, err);
@@ -138,7 +321,7 @@ __device__ void consumer_loop(const P& prob, Shared& sh, unsigned char* stages) 
       break;
     }
     const unsigned char* sp = stages + static_cast<size_t>(stage) * kChunkBytes;
-    const float2 part = prob.consume(mt, sp, &sh.empty[stage], ctid, lane);
+    const float4 part = prob.consume(mt, sp, &sh.empty[stage], ctid, lane);
     if (lane == 0) {
       sh.res_part[rs][warp] = part;
       mbar_arrive(&sh.res_done[rs]);  // release: the partial is visible to the bookkeeper
@@ -146,143 +329,223 @@ __device__ void consumer_loop(const P& prob, Shared& sh, unsigned char* stages) 
   }
 }
 
-// Bookkeeper: book the collected chunks (lane i holds chunk i < nb) and
-// publish completed requests to the finalize list.
+// The bookkeeper: per result slot, combine the consumer warps' partials,
+// store them, and append the chunk's ticket to the booked queue.  It never
+// waits on global memory, so the result ring keeps moving.
 template <class P>
-__device__ void bk_flush(const P& prob, Shared& sh, const PosTables& tab, int lane, int nb,
-                         int e_pos) {
-  if (nb == 0) return;
-  __threadfence();  // the partials -> GPU scope before the tickets
-  bool done = false;
-  if (lane < nb) {
-    const int rows = tab.rstart[e_pos + 1] - tab.rstart[e_pos];
-    const unsigned need = static_cast<unsigned>(rows * prob.ipr);
-    const unsigned old = atomic_add_acq_rel(&prob.ws.tickets[info_req(tab.info[e_pos])], 1u);
-    done = old + 1u == need;
-  }
-  const unsigned dmask = __ballot_sync(0xffffffffu, done);
-  if (dmask) {
-    __threadfence();  // every partial of the completed requests is visible
-    const unsigned tail = sh.fin_tail;
-    // room: the finalizer consumes in order; wait (bounded) if the list is full
-    const unsigned need_room = tail + __popc(dmask);
-    volatile unsigned* vhead = &sh.fin_head;
-    if (need_room - *vhead > static_cast<unsigned>(kFinCap)) {
-      const uint64_t t0 = globaltimer_ns();
-      while (need_room - *vhead > static_cast<unsigned>(kFinCap)) {
-        __nanosleep(200);
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-          if (lane == 0) record_error(&prob.ws.hdr->error, 0x10);
-          break;
-        }
-      }
-    }
-    if (done)
-      reinterpret_cast<volatile int*>(sh.fin_q)[(tail + __popc(dmask & ((1u << lane) - 1u))) %
-                                                 kFinCap] = e_pos;
-    __syncwarp();
-    if (lane == 0) {
-      __threadfence_block();
-      *reinterpret_cast<volatile unsigned*>(&sh.fin_tail) = need_room;
-    }
-  }
-  __syncwarp();
-}
-
-// Bookkeeper warp: per chunk, copy the consumer warps' partials to the
-// workspace (one coalesced 128-byte store; the finalize merges them), then
-// book the chunk's ticket in lane-parallel batches.
-template <class P>
-__device__ void bookkeeper_loop(const P& prob, Shared& sh, const PosTables& tab) {
+__device__ void bookkeeper_loop(const P& prob, Shared& sh) {
   int* err = &prob.ws.hdr->error;
   const int lane = threadIdx.x & 31;
-  int nb = 0;  // chunks collected, not yet booked
-  int e_pos = 0;
   for (int j = 0;; ++j) {
     const int rs = j % kResSlots;
-    const uint32_t par = (j / kResSlots) & 1;
-    if (nb > 0 && !mbar_test_wait(&sh.res_done[rs], par)) {
-      bk_flush(prob, sh, tab, lane, nb, e_pos);
-      nb = 0;
-    }
-    wait_or_flag(sh, &sh.res_done[rs], par, err);
+    wait_or_flag(sh, &sh.res_done[rs], (j / kResSlots) & 1, err);
     const ResMeta rm = sh.res_meta[rs];
     if (rm.item < 0) break;
-    // combine the consumer warps' partials of the chunk (lanes 0..15)
-    const float2 p = lane < kConsumerWarps ? sh.res_part[rs][lane] : make_float2(kNegInf, 0.f);
+    const float4 p = lane < kGroupWarps ? sh.res_part[rs][lane]
+                                        : make_float4(kNegInf, 0.f, 0.f, 0.f);
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.res_free[rs]);
-    float2 tot;
-    if (rm.kind == KIND_ARGMAX) {
-      const VI v = warp_reduce_vi(VI{p.x, lane < kConsumerWarps ? __float_as_int(p.y)
-                                                                : 0x7fffffff});
-      tot = make_float2(v.v, __int_as_float(v.i));
-    } else if (rm.kind == KIND_RESID_PASS) {
-      // residual pass: the partials are segment sums, kept one per warp
-      tot = p;
-    } else {
-      const MS v = warp_reduce_ms(MS{p.x, p.y}, Scale2{rm.c_hi, rm.c_lo});
-      tot = make_float2(v.m, v.s);
-    }
-    const int slot = rm.slot, pos = rm.pos;
     if (rm.kind == KIND_RESID_PASS) {
-      if (lane < kConsumerWarps)
-        prob.ws.partials[static_cast<size_t>(slot) * kConsumerWarps + lane] = tot;
-    } else if (lane == 0) {
-      prob.ws.partials[slot] = tot;
+      // draw-pass chunk: the segment sums of the consumer warps, in order
+      if constexpr (P::kHasDraws) prob.store_segsums(rm, lane, p);
+    } else {
+      float2 tot;
+      if (rm.kind == KIND_ARGMAX) {
+        const VI v = warp_reduce_vi(VI{p.x, lane < kGroupWarps ? __float_as_int(p.y)
+                                                               : 0x7fffffff});
+        tot = make_float2(v.v, __int_as_float(v.i));
+      } else {
+        const MS v = warp_reduce_ms(MS{p.x, p.y}, Scale2{rm.c_hi, rm.c_lo});
+        tot = make_float2(v.m, v.s);
+      }
+      if (lane == 0) prob.ws.partials[rm.slot] = tot;
     }
-    if (lane == nb) e_pos = pos;
-    if (++nb == 32) {
-      bk_flush(prob, sh, tab, lane, nb, e_pos);
-      nb = 0;
+    __syncwarp();  // every lane's stores before lane 0 publishes the entry
+    if (lane == 0) {
+      const unsigned t = sh.bq_tail;
+      if (t - vload(sh.bq_head) >= static_cast<unsigned>(kBqCap)) {
+        const uint64_t t0 = globaltimer_ns();
+        while (t - vload(sh.bq_head) >= static_cast<unsigned>(kBqCap)) {
+          if (globaltimer_ns() - t0 > wait_limit(sh)) {
+            flag_timeout(sh, err);
+            break;
+          }
+          __nanosleep(64);
+        }
+      }
+      sh.bq[t % kBqCap] = make_int4(rm.tkt, rm.need, rm.fin_code, 0);
+      __threadfence_block();
+      *reinterpret_cast<volatile unsigned*>(&sh.bq_tail) = t + 1u;
     }
   }
-  bk_flush(prob, sh, tab, lane, nb, e_pos);
-  __syncwarp();
   if (lane == 0) {
     __threadfence_block();
     *reinterpret_cast<volatile unsigned*>(&sh.bk_done) = 1u;
   }
+  __syncwarp();
+}
+
+// The ticket warp: takes booked chunks in batches of up to 32 (lane i one
+// chunk), makes their partials visible GPU-wide, bumps their tickets and
+// puts each request or draw whose ticket completes on the finalize list.
+// The fence and the atomics' round trip happen here, off the result ring.
+template <class P>
+__device__ void ticketer_loop(const P& prob, Shared& sh) {
+  int* err = &prob.ws.hdr->error;
+  const int lane = threadIdx.x & 31;
+  unsigned head = 0;
+  uint64_t idle_since = 0;
+  unsigned backoff = 32;
+  for (;;) {
+    unsigned tail = vload(sh.bq_tail);
+    if (tail == head) {
+      if (vload(sh.bk_done) != 0u) {
+        __threadfence_block();
+        tail = vload(sh.bq_tail);
+        if (tail == head) break;
+      } else {
+        const uint64_t now = globaltimer_ns();
+        if (idle_since == 0) idle_since = now;
+        if (now - idle_since > 2 * kWaitLimitNs) {
+          if (lane == 0) record_error(err, 0x10);
+          break;
+        }
+        __nanosleep(backoff);
+        backoff = min(backoff * 2u, 256u);
+        continue;
+      }
+    }
+    idle_since = 0;
+    backoff = 32;
+    __threadfence_block();  // the entries (and the bookkeeper's stores) before reading them
+    const int nb = static_cast<int>(min(tail - head, 32u));
+    const int4 e = lane < nb ? sh.bq[(head + lane) % kBqCap] : make_int4(0, 0, 0, 0);
+    __threadfence();  // the partials -> GPU scope before the tickets
+    bool done = false;
+    if (lane < nb) {
+      const unsigned old = atomic_add_acq_rel(&prob.ws.tickets[e.x], 1u);
+      done = old + 1u == static_cast<unsigned>(e.y);
+    }
+    const unsigned dmask = __ballot_sync(0xffffffffu, done);
+    if (dmask) {
+      __threadfence();  // every partial of the completed entries is visible
+      const unsigned ft = sh.fin_tail;
+      // room: wait (bounded) while the list is full
+      const unsigned need_room = ft + __popc(dmask);
+      if (need_room - vload(sh.fin_claim) > static_cast<unsigned>(kFinCap)) {
+        const uint64_t t0 = globaltimer_ns();
+        while (need_room - vload(sh.fin_claim) > static_cast<unsigned>(kFinCap)) {
+          __nanosleep(200);
+          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (lane == 0) record_error(err, 0x10);
+            break;
+          }
+        }
+      }
+      if (done)
+        reinterpret_cast<volatile int*>(sh.fin_q)[(ft + __popc(dmask & ((1u << lane) - 1u))) %
+                                                   kFinCap] = e.z;
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        *reinterpret_cast<volatile unsigned*>(&sh.fin_tail) = need_room;
+      }
+    }
+    head += static_cast<unsigned>(nb);
+    __syncwarp();
+    if (lane == 0) *reinterpret_cast<volatile unsigned*>(&sh.bq_head) = head;
+  }
+  if (lane == 0) {
+    __threadfence_block();
+    *reinterpret_cast<volatile unsigned*>(&sh.tk_done) = 1u;
+  }
+  __syncwarp();
+}
+
+// Take the next finalize-list entry: returns it, -2 when the CTA is done,
+// -1 when there is nothing yet.  Marks the caller busy while it holds one.
+__device__ __forceinline__ int fin_take(Shared& sh) {
+  const unsigned c = vload(sh.fin_claim);
+  if (c != vload(sh.fin_tail)) {
+    atomicAdd(&sh.fin_busy, 1u);
+    if (atomicCAS(&sh.fin_claim, c, c + 1u) == c) {
+      __threadfence_block();
+      return reinterpret_cast<volatile int*>(sh.fin_q)[c % kFinCap];
+    }
+    atomicSub(&sh.fin_busy, 1u);
+    return -1;
+  }
+  if (vload(sh.tk_done) != 0u && vload(sh.fin_claim) == vload(sh.fin_tail)) return -2;
+  return -1;
+}
+
+__device__ __forceinline__ void fin_release(Shared& sh) {
+  __threadfence_block();
+  atomicSub(&sh.fin_busy, 1u);
 }
 
 template <class P>
 __device__ void finalizer_loop(const P& prob, Shared& sh, const PosTables& tab) {
   const int ftid = threadIdx.x - kFinBase;
+  const int fwarp = ftid >> 5, lane = ftid & 31;
   uint64_t idle_since = 0;
   unsigned backoff = 32;
-  for (;;) {
-    if (ftid == 0) {
-      int cmd = -1;  // idle
-      volatile unsigned* vtail = &sh.fin_tail;
-      const unsigned tail = *vtail;
-      if (sh.fin_head != tail) {
-        __threadfence_block();
-        cmd = reinterpret_cast<volatile int*>(sh.fin_q)[sh.fin_head % kFinCap];
-        *reinterpret_cast<volatile unsigned*>(&sh.fin_head) = sh.fin_head + 1u;
-        idle_since = 0;
-        backoff = 32;
-      } else if (*reinterpret_cast<volatile unsigned*>(&sh.bk_done) != 0u &&
-                 *vtail == sh.fin_head) {
-        cmd = -2;  // every chunk booked and every complete request finalized
-      } else {
-        const uint64_t now = globaltimer_ns();
-        if (idle_since == 0) idle_since = now;
-        if (now - idle_since > 2 * kWaitLimitNs) {
-          record_error(&prob.ws.hdr->error, 0x10);
-          cmd = -2;
+  if constexpr (P::kWarpFinalize) {
+    for (;;) {
+      int cmd = -1;
+      if (lane == 0) {
+        cmd = fin_take(sh);
+        if (cmd == -1) {
+          const uint64_t now = globaltimer_ns();
+          if (idle_since == 0) idle_since = now;
+          if (now - idle_since > 2 * kWaitLimitNs) {
+            record_error(&prob.ws.hdr->error, 0x10);
+            cmd = -2;
+          }
+        } else {
+          idle_since = 0;
         }
       }
-      if (cmd == -1) {
+      cmd = __shfl_sync(0xffffffffu, cmd, 0);
+      if (cmd == -2) break;
+      if (cmd >= 0) {
+        prob.finalize_warp(sh, tab, cmd, lane, sh.wfin[fwarp]);
+        __syncwarp();
+        if (lane == 0) fin_release(sh);
+        backoff = 32;
+      } else {
         __nanosleep(backoff);
         backoff = min(backoff * 2u, 256u);
       }
-      sh.fin_cmd = cmd;
     }
-    named_sync(1, kFinThreads);
-    const int cmd = sh.fin_cmd;
-    named_sync(1, kFinThreads);
-    if (cmd == -2) break;
-    if (cmd >= 0) prob.finalize(sh, tab, cmd, ftid);
+  } else {
+    for (;;) {
+      if (ftid == 0) {
+        int cmd = fin_take(sh);
+        if (cmd == -1) {
+          const uint64_t now = globaltimer_ns();
+          if (idle_since == 0) idle_since = now;
+          if (now - idle_since > 2 * kWaitLimitNs) {
+            record_error(&prob.ws.hdr->error, 0x10);
+            cmd = -2;
+          }
+          __nanosleep(backoff);
+          backoff = min(backoff * 2u, 256u);
+        } else {
+          idle_since = 0;
+          backoff = 32;
+        }
+        sh.fin_cmd = cmd;
+      }
+      named_sync(1, kFinThreads);
+      const int cmd = sh.fin_cmd;
+      named_sync(1, kFinThreads);
+      if (cmd == -2) break;
+      if (cmd >= 0) {
+        prob.finalize(sh, tab, cmd, ftid);
+        if (ftid == 0) fin_release(sh);
+      }
+    }
   }
 }
 
@@ -306,38 +569,56 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const P prob) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sh.full[s], 1);
-      mbar_init(&sh.empty[s], kConsumerWarps);
+      mbar_init(&sh.empty[s], kGroupWarps);
     }
     for (int s = 0; s < kResSlots; ++s) {
-      mbar_init(&sh.res_done[s], kConsumerWarps + 1);
+      mbar_init(&sh.res_done[s], kGroupWarps + 1);
       mbar_init(&sh.res_free[s], 1);
     }
     fence_mbar_init();
     sh.timed_out = 0;
-    sh.fin_head = sh.fin_tail = 0u;
+    sh.fin_claim = sh.fin_tail = sh.fin_busy = 0u;
     sh.bk_done = 0u;
+    sh.bq_tail = sh.bq_head = 0u;
+    sh.tk_done = 0u;
     sh.fin_cmd = -1;
+    sh.n_draw_cap = 0;
   }
   prob.preamble(sh, tab, scan_tmp);
   __syncthreads();
 
-  if (threadIdx.x < kConsumers) {
-    consumer_loop(prob, sh, stages);
-  } else if (threadIdx.x < kBkBase) {
-    if (threadIdx.x == kProducerThread) producer_loop(prob, sh, tab, stages);
+  if (threadIdx.x < kBkBase) {
+    producer_loop(prob, sh, tab, stages);
+  } else if (threadIdx.x < kTkBase) {
+    bookkeeper_loop(prob, sh);
   } else if (threadIdx.x < kFinBase) {
-    bookkeeper_loop(prob, sh, tab);
-  } else {
+    ticketer_loop(prob, sh);
+  } else if (threadIdx.x < kConsBase) {
     finalizer_loop(prob, sh, tab);
+  } else {
+    consumer_loop(prob, sh, stages);
   }
   __syncthreads();
+  // the last CTA to finish leaves the shared counters zeroed for the next call
   if (threadIdx.x == 0) {
     __threadfence();
     const unsigned d = atomicAdd(&prob.ws.hdr->done_ctas, 1u);
-    if (d + 1u == gridDim.x) {
-      prob.ws.hdr->work_counter = 0u;
-      prob.ws.hdr->done_ctas = 0u;
-      prob.last_cta_reset();
+    sh.is_last = d + 1u == gridDim.x ? 1 : 0;
+    if (sh.is_last) __threadfence();
+  }
+  __syncthreads();
+  if (sh.is_last) {
+    WsHeader* hdr = prob.ws.hdr;
+    const int nd = min(static_cast<int>(*reinterpret_cast<volatile unsigned*>(&hdr->draw_reserve)),
+                       prob.n_req);
+    for (int i = threadIdx.x; i < nd; i += kThreads) prob.ws.draws[i] = 0;
+    prob.last_cta_reset();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      hdr->work_counter = 0u;
+      hdr->done_ctas = 0u;
+      hdr->draw_reserve = 0u;
+      hdr->fin_count = 0u;
       __threadfence();
     }
   }

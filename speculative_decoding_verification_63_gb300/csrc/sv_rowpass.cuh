@@ -23,63 +23,105 @@ constexpr int kStages = 4;
 constexpr int kChunkBytes = 32768;
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kVecPerThread = kChunkBytes / 16 / kConsumers;  // 16-byte vectors per chunk
+constexpr int kGroups = 2;                    // consumer groups, taking alternate chunks
+constexpr int kGroupWarps = kConsumerWarps / kGroups;
+constexpr int kGroupThreads = kGroupWarps * 32;
+constexpr int kVecPerThread = kChunkBytes / 16 / kGroupThreads;  // 16-byte vectors per chunk
 constexpr int kResSlots = 16;                 // result ring (consumers -> bookkeeper)
 constexpr int kFinWarps = 4;                  // finalizer group
 constexpr int kFinThreads = kFinWarps * 32;
-constexpr int kProducerThread = kConsumers;   // lane 0 of the producer warp
-constexpr int kBkBase = kConsumers + 32;      // bookkeeper warp
-constexpr int kFinBase = kConsumers + 64;     // finalizer group
-constexpr int kThreads = kFinBase + kFinThreads;
+// Warp roles.  The control warps come first: the warp schedulers favour
+// lower warp ids among ready warps, and the consumers are ready almost
+// always, so control work placed after them would wait for gaps.
+constexpr int kProducerBase = 0;              // the producer warp
+constexpr int kBkBase = 32;                   // bookkeeper warp
+constexpr int kTkBase = 64;                   // ticket warp
+constexpr int kFinBase = 96;                  // finalizer group
+constexpr int kConsBase = kFinBase + kFinThreads;  // consumer warps
+constexpr int kThreads = kConsBase + kConsumers;
+constexpr int kRSeg = 256;                   // draw pass: tokens per segment (8 per lane)
+constexpr int kPageSeg = 512;                // draw finalize: segments per page (16 per lane)
+constexpr int kMaxPages = 8;                 // => at most 4096 segments (V <= 2^20)
 constexpr int kFinCap = 128;                  // requests awaiting their finalize
+constexpr int kBqCap = 256;                   // booked chunks awaiting their ticket
 constexpr int kSegEl = 1024;        // inverse-CDF segment: 32 lanes x 32 elements
 constexpr int kMaxSeg = 1024;       // => V <= 2^20
 constexpr int kMaxRowsPerReq = 128;  // chain: 2K+1 <= 65; tree: N + M <= 128
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 constexpr uint64_t kWaitLimitAfterTimeoutNs = 1000000ull;  // 1 ms
 
-static_assert(kVecPerThread * 16 * kConsumers == kChunkBytes, "chunk split");
+static_assert(kVecPerThread * 16 * kGroupThreads == kChunkBytes, "chunk split");
+static_assert(kStages % kGroups == 0, "each group owns whole stages");
+static_assert(kVecPerThread == 4 || kVecPerThread == 8, "the bf16 reduction's sum tree");
+// draw pass: 256-token segments per consumer warp and chunk
+constexpr int kSpwBf16 = kChunkBytes / 2 / 2 / kRSeg / kGroupWarps;
+constexpr int kSpwF32 = kChunkBytes / 2 / 4 / kRSeg / kGroupWarps;
+static_assert(kSpwF32 >= 1 && kSpwBf16 <= 4, "draw-pass segments per warp");
 
 enum RowKind : int { KIND_ARGMAX = 0, KIND_SOFTMAX = 1, KIND_TOPK = 2, KIND_RESID_PASS = 3 };
 
+constexpr int kFinResid = 0x40000000;  // finalize-list flag: a residual draw (request id below)
+constexpr int kDrawSlot = 32;                // producer plan entry of a draw-pass chunk
+constexpr int kDrawTicketBase = 1024;  // draw tickets follow the request tickets (SV_MAX_B)
+
 struct WsHeader {
-  unsigned int work_counter;
+  unsigned int work_counter;  // chunks claimed: main pass, then draw pass
   unsigned int done_ctas;
   int error;
-  int n_jobs;  // residual-pass jobs left by the chain pass (reset by the residual pass)
+  unsigned int draw_reserve;  // draws published so far (entries of the draw list)
+  unsigned int fin_count;     // requests whose finalize has run (or that failed up front)
+  unsigned int pad[3];
 };
 
 // Device view of the caller's workspace.
 struct Ws {
   WsHeader* hdr;
-  unsigned int* tickets;  // [SV_MAX_B]
-  float2* partials;       // [rows_max * ipr * kConsumerWarps]
+  unsigned int* tickets;  // [2 SV_MAX_B] chunk counters: requests, then their draws
+  int* draws;             // [SV_MAX_B] draw list: request id + 1, 0 = not yet written
+  float2* partials;       // [rows_max * ipr] one (max, sum) / (max, argmax) per chunk
+  float* segsums;         // [B * ipr2 * segments per chunk] residual segment sums
   float* scratch;         // per-request residual rows (tree walk) [B][2][V]
-  void* jobs;             // residual-pass jobs [SV_MAX_B]
+  void* jobs;             // residual draws [SV_MAX_B]
+};
+
+// A residual / bonus draw (CMU 15-779 Lecture 17, sec. 2.3-2.4): request b,
+// position n, mode 0: w = max(0, p_n - q_n), mode 1: w = p_n; the row
+// statistics of p_n and q_n, and the temperature scale.
+struct P2Job {
+  int b, n, mode;
+  float mp, izp, mq, izq;
+  float c_hi, c_lo;
+  int pad[3];
 };
 
 struct StageMeta {
   int item;      // -1: no more work
-  int pos;       // request position in processing order
-  int row;       // flat row id (processing order)
+  int pos;       // request position in processing order (main pass)
   int kind;
   int n_el;      // elements in this chunk
   int el_base;   // first element's index within the row
   float c_hi, c_lo;
   const char* src;   // first element of the chunk
   const char* src2;  // second row's chunk (residual pass), or null
-  float4 aux;        // problem-specific constants of the chunk
-  int sub;           // problem-specific small value (residual pass: mode)
+  float4 aux;        // residual pass: mp, 1/Zp, mq, 1/Zq
+  int sub;           // residual pass: mode
 };
 
 // What the bookkeeper needs about a result slot.
 struct ResMeta {
-  int item;  // -1: no more work
-  int pos;
-  int slot;  // partial index: row * ipr + chunk
+  int item;      // -1: no more work
   int kind;
+  int slot;      // where the chunk's partial(s) go
+  int tkt;       // ticket (request id)
+  int need;      // ticket value that completes the request / draw
+  int fin_code;  // finalize-list entry on completion
   float c_hi, c_lo;
 };
+
+static_assert(sizeof(StageMeta) % 4 == 0 && sizeof(ResMeta) == 32, "meta copied by words");
+constexpr int kMetaWords = sizeof(StageMeta) / 4;
+constexpr int kResWords = sizeof(ResMeta) / 4;
+static_assert(kMetaWords + kResWords <= 32, "one word per producer lane");
 
 struct FinScratch {
   double dsum[kFinWarps];
@@ -96,6 +138,13 @@ struct FinScratch {
   int misc[8];
 };
 
+// Row statistics of one request, private to one finalizer warp.
+struct WarpFin {
+  float rm[kMaxRowsPerReq];
+  float rz[kMaxRowsPerReq];
+  int ridx[kMaxRowsPerReq];
+};
+
 struct __align__(16) Shared {
   uint64_t full[kStages];      // producer -> consumers: chunk landed (tx bytes)
   uint64_t empty[kStages];     // consumers -> producer: chunk in registers
@@ -103,15 +152,25 @@ struct __align__(16) Shared {
   uint64_t res_free[kResSlots];  // bookkeeper -> producer: slot consumed
   StageMeta meta[kStages];
   ResMeta res_meta[kResSlots];
-  float2 res_part[kResSlots][kConsumerWarps];
+  StageMeta plan_m[33];         // the producer warp's next chunks, worked out together;
+  ResMeta plan_r[33];           // entry kDrawSlot: the next draw-pass chunk
+  float4 res_part[kResSlots][kGroupWarps];
+  int4 bq[kBqCap];             // booked chunks: ticket, count that completes it, finalize code
+  unsigned bq_tail;            // entries published (bookkeeper only)
+  unsigned bq_head;            // entries ticketed (ticket warp only)
+  unsigned tk_done;            // the ticket warp has ticketed every chunk
   int fin_q[kFinCap];
-  unsigned fin_head;           // next entry the finalizer takes (finalizer only)
-  unsigned fin_tail;           // entries published (bookkeeper only)
+  unsigned fin_claim;          // finalize-list entries taken (finalizer warps, CAS)
+  unsigned fin_tail;           // entries published (ticket warp only)
+  unsigned fin_busy;           // finalizer warps inside a finalize
   unsigned bk_done;            // the bookkeeper has booked every chunk
-  int fin_cmd;                 // finalizer group command: pos, -1 idle, -2 exit
+  int fin_cmd;                 // group finalize command: pos, -1 idle, -2 exit
   int n_pos;
+  int n_draw_cap;   // at most this many draws can be published (sampled requests)
   int timed_out;  // a bounded wait of this CTA expired: later waits are short
+  int is_last;    // this CTA finished last
   FinScratch fin;
+  WarpFin wfin[kFinWarps];
 };
 
 // Per-position tables that follow Shared in dynamic shared memory.
@@ -203,7 +262,7 @@ __device__ __forceinline__ void reduce_chunk_bf16(const StageMeta& mt, const uin
   uint4 r[kVecPerThread];
 #pragma unroll
   for (int k = 0; k < kVecPerThread; ++k) {
-    const int v = ctid + k * kConsumers;
+    const int v = ctid + k * kGroupThreads;
     r[k] = v < nvec ? stage[v] : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
   }
   __syncwarp();
@@ -236,7 +295,10 @@ __device__ __forceinline__ void reduce_chunk_bf16(const StageMeta& mt, const uin
         }
         sk[k] = acc;
       }
-      s = (sk[0] + sk[1]) + (sk[2] + sk[3]);
+      if constexpr (kVecPerThread == 8)
+        s = ((sk[0] + sk[1]) + (sk[2] + sk[3])) + ((sk[4] + sk[5]) + (sk[6] + sk[7]));
+      else
+        s = (sk[0] + sk[1]) + (sk[2] + sk[3]);
     }
     ms = MS{m, s};
   } else {
@@ -244,7 +306,7 @@ __device__ __forceinline__ void reduce_chunk_bf16(const StageMeta& mt, const uin
     if (m == m) {
 #pragma unroll
       for (int k = 0; k < kVecPerThread; ++k) {
-        const int v = ctid + k * kConsumers;
+        const int v = ctid + k * kGroupThreads;
         const uint32_t w[4] = {r[k].x, r[k].y, r[k].z, r[k].w};
         int cand = 0x7fffffff;
 #pragma unroll
@@ -275,7 +337,7 @@ __device__ __forceinline__ void reduce_chunk_generic(const StageMeta& mt, const 
   float m = kNegInf;
   bool bad = false;
   int idx = 0x7fffffff;
-  for (int e = ctid; e < mt.n_el; e += kConsumers) {
+  for (int e = ctid; e < mt.n_el; e += kGroupThreads) {
     const float x = ld(e);
     if (x != x || x == kPosInf) bad = true;
     if (idx == 0x7fffffff || x > m) {
@@ -287,7 +349,7 @@ __device__ __forceinline__ void reduce_chunk_generic(const StageMeta& mt, const 
     float s = 0.f;
     if (!bad && m != kNegInf) {
       const Scale2 c{mt.c_hi, mt.c_lo};
-      for (int e = ctid; e < mt.n_el; e += kConsumers) s += fast_exp2(scaled_arg(ld(e), m, c));
+      for (int e = ctid; e < mt.n_el; e += kGroupThreads) s += fast_exp2(scaled_arg(ld(e), m, c));
     }
     ms = bad ? MS{nan_f(), 0.f} : MS{m, s};
   } else {
@@ -323,6 +385,35 @@ __device__ __forceinline__ float2 reduce_row_chunk(const StageMeta& mt, const un
                                        empty_bar, ctid, lane, ms, vi);
   ms = warp_reduce_ms(ms, Scale2{mt.c_hi, mt.c_lo});
   return make_float2(ms.m, ms.s);
+}
+
+// ------------------------------------------------------ residual weights
+
+struct ResidParams {
+  float mp, izp, mq, izq;
+  Scale2 c;
+  int mode;  // 0: max(0, p - q); 1: unnormalised p
+};
+
+// Residual weight of one token from its two logits.  Every operation is an
+// explicitly rounded intrinsic, so the chunk pass and the final rescan
+// produce the same bits.
+__device__ __forceinline__ float resid_weight(float xp, float xq, const ResidParams& r) {
+  const float dp = fmaxf(__fsub_rn(xp, r.mp), -1.0e30f);
+  const float ep = fast_exp2(__fmaf_rn(dp, r.c.hi, __fmul_rn(dp, r.c.lo)));
+  if (r.mode != 0) return ep;
+  const float dq = fmaxf(__fsub_rn(xq, r.mq), -1.0e30f);
+  const float eq = fast_exp2(__fmaf_rn(dq, r.c.hi, __fmul_rn(dq, r.c.lo)));
+  return fmaxf(__fsub_rn(__fmul_rn(ep, r.izp), __fmul_rn(eq, r.izq)), 0.f);
+}
+
+__device__ __forceinline__ float warp_incl_scan_rn(float x, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x = __fadd_rn(x, y);
+  }
+  return x;
 }
 
 // ---------------------------------------------------------- inverse CDF
@@ -473,6 +564,61 @@ __device__ __forceinline__ void load32(const char* row, int es, bool vec_ok, int
 __device__ __forceinline__ float load_logit(const char* row, int es, int t) {
   return es == 2 ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(row)[t])
                  : reinterpret_cast<const float*>(row)[t];
+}
+
+// Eight consecutive logits [t0, t0 + 8) of a row piece holding n valid
+// entries; entries at or beyond n read as -inf.  With vec the piece is
+// 16-byte aligned and may be read in whole 16-byte vectors up to n rounded
+// up to a vector (a staged chunk, or an aligned row of 16-byte multiple
+// length); otherwise entries are read one by one.
+__device__ __forceinline__ void load8(const char* base, int es, bool vec, int t0, int n,
+                                      float* x) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) x[j] = kNegInf;
+  if (t0 >= n) return;
+  if (vec && es == 2) {
+    const uint4 v = *reinterpret_cast<const uint4*>(base + static_cast<size_t>(t0) * 2);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      x[2 * h] = bf16lo(w[h]);
+      x[2 * h + 1] = bf16hi(w[h]);
+    }
+  } else if (vec) {
+    const float4 a = *reinterpret_cast<const float4*>(base + static_cast<size_t>(t0) * 4);
+    x[0] = a.x;
+    x[1] = a.y;
+    x[2] = a.z;
+    x[3] = a.w;
+    if (t0 + 4 < n) {
+      const float4 c = *reinterpret_cast<const float4*>(base + static_cast<size_t>(t0) * 4 + 16);
+      x[4] = c.x;
+      x[5] = c.y;
+      x[6] = c.z;
+      x[7] = c.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (t0 + j < n) x[j] = load_logit(base, es, t0 + j);
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if (t0 + j >= n) x[j] = kNegInf;
+}
+
+// Residual weights of eight tokens and their sequential fp32 sum; tokens at
+// or beyond n weigh 0.  The draw pass and the final rescan both go through
+// here, so they produce the same bits.
+__device__ __forceinline__ float resid_weights8(const float* xp, const float* xq, int t0, int n,
+                                                const ResidParams& r, float* w) {
+  float ls = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    w[j] = t0 + j < n ? resid_weight(xp[j], xq[j], r) : 0.f;
+    ls = __fadd_rn(ls, w[j]);
+  }
+  return ls;
 }
 
 }  // namespace sv

@@ -18,6 +18,8 @@ namespace sv {
 
 struct TreeProblem {
   static constexpr int kAuxBytes = 8;
+  static constexpr bool kWarpFinalize = false;
+  static constexpr bool kHasDraws = false;
   int n_req, N, M, V, max_depth, es, ipr, chunk_el, max_topk;
   bool bulk;
   const char* target;
@@ -117,7 +119,7 @@ struct TreeProblem {
     }
   }
 
-  __device__ void fill_stage(const PosTables& tab, int rl, StageMeta& mt) const {
+  __device__ void fill_stage(const PosTables& tab, int rl, StageMeta& mt, ResMeta& rm) const {
     const int info = tab.info[mt.pos];
     const int b = info_req(info), nn = info_extra(info);
     mt.kind = info_kind(info);
@@ -135,11 +137,17 @@ struct TreeProblem {
       rp = draft + (static_cast<int64_t>(b) * M + r) * d_stride;
     }
     mt.src = rp + static_cast<size_t>(mt.el_base) * es;
+    rm.tkt = b;
+    rm.need = (tab.rstart[mt.pos + 1] - tab.rstart[mt.pos]) * ipr;
+    rm.fin_code = mt.pos;
   }
 
-  __device__ float2 consume(const StageMeta& mt, const unsigned char* sp, uint64_t* empty_bar,
+  // trees draw inside their walk: no separate draw pass
+
+  __device__ float4 consume(const StageMeta& mt, const unsigned char* sp, uint64_t* empty_bar,
                             int ctid, int lane) const {
-    return reduce_row_chunk(mt, sp, empty_bar, ctid, lane, bulk, es);
+    const float2 r = reduce_row_chunk(mt, sp, empty_bar, ctid, lane, bulk, es);
+    return make_float4(r.x, r.y, 0.f, 0.f);
   }
 
   __device__ static unsigned long long ref_of(const PosTables& tab, int pos) {
@@ -147,6 +155,7 @@ struct TreeProblem {
   }
 
   __device__ void finalize(Shared& sh, const PosTables& tab, int pos, int ftid) const;
+  __device__ void finalize_warp(Shared&, const PosTables&, int, int, WarpFin&) const {}
   __device__ void last_cta_reset() const {}
 };
 
