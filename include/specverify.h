@@ -199,6 +199,38 @@ sv_status sv_get_error(void* workspace, sv_stream_t stream, int32_t* device_flag
 sv_status sv_selftest_wait_timeout(void* workspace, size_t ws_bytes,
                                    int64_t limit_ns, sv_stream_t stream);
 
+/* ---- Allocation-free chain entry point (no counterpart on the pages) ----
+ *
+ * For callers that cannot hand the library a workspace buffer: a host
+ * program with no device allocator of its own at the call site, or a call
+ * site where allocating device memory is not allowed or could block.  The
+ * scratch these calls use is one file-scope device array per device,
+ * SV_NOALLOC_SCRATCH_BYTES long, reserved when the library's module loads;
+ * the calls themselves allocate nothing.
+ *
+ *   - The first call on a device (with that device current) looks up the
+ *     array's address (cudaGetSymbolAddress) and zeroes it on `stream`
+ *     (cudaMemsetAsync), ahead of the kernel; make that first call before
+ *     any stream capture that should contain only the verification.
+ *   - A call whose sv_chain_workspace_bytes(...) exceeds
+ *     SV_NOALLOC_SCRATCH_BYTES is rejected with SV_EWORKSPACE before any
+ *     device work; use sv_verify_chain with a caller workspace instead.
+ *   - The counters at the start of the scratch must be zero when a call
+ *     starts; every call leaves them zero.  sv_noalloc_get_error re-zeroes
+ *     the scratch (on `stream`) after reporting a device error.
+ *   - All calls on one device share the one scratch: calls that may overlap
+ *     on the GPU (e.g. on different streams without ordering) race and give
+ *     undefined results.  Order them, or use sv_verify_chain with separate
+ *     workspaces.
+ * Arguments, layouts and results are those of sv_verify_chain. */
+#define SV_NOALLOC_SCRATCH_BYTES (8u << 20) /* 8 MiB per device */
+
+sv_status sv_verify_chain_noalloc(const sv_chain_args* args, sv_stream_t stream);
+
+/* sv_get_error for the allocation-free scratch of the current device; after
+   a device error it also re-zeroes the scratch on `stream`. */
+sv_status sv_noalloc_get_error(sv_stream_t stream, int32_t* device_flags);
+
 const char* sv_status_string(sv_status status);
 
 /* Library version, major*10000 + minor*100 + patch. */

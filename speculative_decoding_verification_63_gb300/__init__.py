@@ -19,7 +19,8 @@ from ._binding import (  # noqa: F401
     SV_EWORKSPACE, SV_FP32, SV_MAX_B, SV_MAX_K, SV_MAX_TOPK, SV_MAX_TREE_B,
     SV_MAX_TREE_NODES, SV_MAX_V, SV_OK, SpecVerifyError, lib, sv_chain_workspace_bytes,
     sv_get_error, sv_selftest_wait_timeout, sv_status_string, sv_tree_workspace_bytes,
-    sv_verify_chain, sv_verify_tree, sv_version, sv_workspace_init)
+    sv_verify_chain, sv_verify_tree, sv_version, sv_workspace_init,
+    SV_NOALLOC_SCRATCH_BYTES, sv_noalloc_get_error, sv_verify_chain_noalloc)
 from ._build import build_library  # noqa: F401
 
 _ws_lock = threading.Lock()

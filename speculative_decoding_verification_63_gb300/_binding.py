@@ -25,7 +25,9 @@ SV_MAX_TREE_NODES, SV_MAX_TREE_B = 64, 1024
 # every symbol include/specverify.h declares
 EXPORTS = ("sv_chain_workspace_bytes", "sv_tree_workspace_bytes", "sv_workspace_init",
            "sv_verify_chain", "sv_verify_tree", "sv_get_error", "sv_selftest_wait_timeout",
+           "sv_verify_chain_noalloc", "sv_noalloc_get_error",
            "sv_status_string", "sv_version")
+SV_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 _P = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -92,6 +94,10 @@ def lib(path: str | None = None):
     h.sv_get_error.restype = ctypes.c_int
     h.sv_selftest_wait_timeout.argtypes = [_P, ctypes.c_size_t, _i64, _P]
     h.sv_selftest_wait_timeout.restype = ctypes.c_int
+    h.sv_verify_chain_noalloc.argtypes = [ctypes.POINTER(SvChainArgs), _P]
+    h.sv_verify_chain_noalloc.restype = ctypes.c_int
+    h.sv_noalloc_get_error.argtypes = [_P, ctypes.POINTER(_i32)]
+    h.sv_noalloc_get_error.restype = ctypes.c_int
     h.sv_status_string.argtypes = [ctypes.c_int]
     h.sv_status_string.restype = ctypes.c_char_p
     h.sv_version.argtypes = []
@@ -270,3 +276,61 @@ def sv_selftest_wait_timeout(workspace, limit_ns: int, stream=None) -> int:
     return lib().sv_selftest_wait_timeout(_ptr(workspace),
                                           workspace.numel() * workspace.element_size(),
                                           int(limit_ns), _stream(stream))
+
+
+# ------------------------------------------------ allocation-free chain call
+
+def sv_verify_chain_noalloc(target_logits, draft_logits, draft_tokens, temperature, uniforms,
+                            out_tokens, out_len, accept_len, num_drafts=None, top_k=None,
+                            max_top_k: int = 0, p_at_draft=None, q_at_draft=None,
+                            stream=None) -> None:
+    """Enqueue sv_verify_chain_noalloc: the chain verification with the
+    library's own per-device scratch (no workspace argument)."""
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    a = SvChainArgs()
+    a.B, a.K, a.V = B, K, V
+    a.dtype = _dtype_code(target_logits)
+    a.target_logits = _ptr(target_logits)
+    a.target_row_stride = _row_stride(target_logits, K1)
+    if draft_logits is not None:
+        if draft_logits.dtype != target_logits.dtype or tuple(draft_logits.shape) != (B, K, V):
+            raise ValueError("draft_logits must be [B][K][V] of the target's dtype")
+        if draft_logits.numel() > 0:
+            a.draft_logits = _ptr(draft_logits)
+            a.draft_row_stride = _row_stride(draft_logits, K)
+    if draft_tokens is not None and draft_tokens.numel() == 0:
+        draft_tokens = None
+    for t, dt, shp, nm in [(draft_tokens, torch.int32, (B, K), "draft_tokens"),
+                           (temperature, torch.float32, (B,), "temperature"),
+                           (uniforms, torch.float32, (B, K + 1), "uniforms"),
+                           (num_drafts, torch.int32, (B,), "num_drafts"),
+                           (top_k, torch.int32, (B,), "top_k"),
+                           (out_tokens, torch.int32, (B, K + 1), "out_tokens"),
+                           (out_len, torch.int32, (B,), "out_len"),
+                           (accept_len, torch.int32, (B,), "accept_len"),
+                           (p_at_draft, torch.float32, (B, K), "p_at_draft"),
+                           (q_at_draft, torch.float32, (B, K), "q_at_draft")]:
+        _check(t, dt, shp, nm)
+    a.draft_tokens, a.num_drafts = _ptr(draft_tokens), _ptr(num_drafts)
+    a.temperature, a.top_k, a.max_top_k = _ptr(temperature), _ptr(top_k), max_top_k
+    a.uniforms = _ptr(uniforms)
+    a.out_tokens, a.out_len, a.accept_len = _ptr(out_tokens), _ptr(out_len), _ptr(accept_len)
+    a.p_at_draft, a.q_at_draft = _ptr(p_at_draft), _ptr(q_at_draft)
+    st = lib().sv_verify_chain_noalloc(ctypes.byref(a), _stream(stream))
+    if st == SV_EWORKSPACE:
+        need = sv_chain_workspace_bytes(B, K, V, a.dtype, max_top_k)
+        raise SpecVerifyError(st, f"sv_verify_chain_noalloc: the call needs {need} bytes of "
+                                  f"scratch, more than SV_NOALLOC_SCRATCH_BYTES "
+                                  f"({SV_NOALLOC_SCRATCH_BYTES}); use sv_verify_chain with a "
+                                  "workspace")
+    if st != SV_OK:
+        raise SpecVerifyError(st, "sv_verify_chain_noalloc")
+
+
+def sv_noalloc_get_error(stream=None) -> tuple[int, int]:
+    """(status, device flags) of the allocation-free scratch of the current
+    device; synchronises the stream; re-zeroes the scratch after an error."""
+    flags = _i32(0)
+    st = lib().sv_noalloc_get_error(_stream(stream), ctypes.byref(flags))
+    return st, flags.value

@@ -142,6 +142,42 @@ __global__ void wait_selftest_kernel(WsHeader* hdr, uint64_t limit_ns) {
 
 }  // namespace
 
+// ------------------------------------------------- allocation-free scratch
+
+// Callers that cannot pass a workspace -- no device allocator at hand where
+// they call, or a call site where allocating device memory is not allowed or
+// could block -- get this per-device array instead.  It is reserved when the
+// module loads; the entry point below only looks up its address once per
+// device and never allocates.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SV_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+struct NoallocSlot {
+  void* ptr = nullptr;
+};
+NoallocSlot g_noalloc[64];
+
+// The scratch of the current device; the first call for a device looks up
+// its address and zeroes it on `stream` (ahead of whatever follows there).
+sv_status noalloc_scratch(cudaStream_t stream, void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ECUDA;
+  if (dev < 0 || dev >= 64) return SV_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_noalloc[dev].ptr == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return SV_ECUDA;
+    if (cudaMemsetAsync(p, 0, SV_NOALLOC_SCRATCH_BYTES, stream) != cudaSuccess) return SV_ECUDA;
+    g_noalloc[dev].ptr = p;
+  }
+  *out = g_noalloc[dev].ptr;
+  return SV_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int32_t sv_version(void) { return 100; }
@@ -338,6 +374,37 @@ sv_status sv_selftest_wait_timeout(void* workspace, size_t ws_bytes, int64_t lim
                                         static_cast<uint64_t>(limit_ns));
   if (cudaGetLastError() != cudaSuccess) return SV_ECUDA;
   return sv_get_error(workspace, stream, nullptr);
+}
+
+
+sv_status sv_verify_chain_noalloc(const sv_chain_args* a, sv_stream_t stream) {
+  if (a == nullptr) return SV_EINVAL;
+  if (a->B == 0) return sv_verify_chain(a, nullptr, 0, stream);
+  const size_t need = sv_chain_workspace_bytes(a->B, a->K, a->V, a->dtype, a->max_top_k);
+  if (need == 0) return SV_EINVAL;
+  if (need > SV_NOALLOC_SCRATCH_BYTES) return SV_EWORKSPACE;  // too large for the scratch
+  DeviceInfo dev;
+  const sv_status ds = device_info(dev);
+  if (ds != SV_OK) return ds;
+  void* ws = nullptr;
+  const sv_status st = noalloc_scratch(reinterpret_cast<cudaStream_t>(stream), &ws);
+  if (st != SV_OK) return st;
+  return sv_verify_chain(a, ws, SV_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+sv_status sv_noalloc_get_error(sv_stream_t stream, int32_t* device_flags) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  const sv_status st = noalloc_scratch(s, &ws);
+  if (st != SV_OK) return st;
+  const sv_status es = sv_get_error(ws, stream, device_flags);
+  if (es == SV_EDATA || es == SV_ETIMEOUT) {
+    // a failed call may leave counters set: start the next one from zero
+    if (cudaMemsetAsync(ws, 0, SV_NOALLOC_SCRATCH_BYTES, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return SV_ECUDA;
+  }
+  return es;
 }
 
 }  // extern "C"
