@@ -122,10 +122,7 @@ struct ChainProblem {
       tab.info[pos] = make_info(b, kind < 0 ? 0 : kind, nd < 0 ? 0 : min(nd, 0x7ff));
       const Scale2 c = scale_for(temperature[b]);
       tab.scale[pos] = make_float2(c.hi, c.lo);
-      if (kind < 0 && blockIdx.x == 0) {
-        write_failed(b, 0x20);
-        atomicAdd(&ws.hdr->fin_count, 1u);  // never finalized: counted here
-      }
+      if (kind < 0 && blockIdx.x == 0) write_failed(b, 0x20);
     }
     if (threadIdx.x == 0) {
       tab.rstart[n_req] = tot.y + tot.w;
@@ -436,24 +433,31 @@ __device__ void ChainProblem::request_finalize(Shared& sh, const PosTables& tab,
     accept_len[b] = err ? 0 : n;
     if (err) record_error(&ws.hdr->error, err);
     ws.tickets[b] = 0u;  // ready for the next call
-    if (!err && !greedy) {
-      // the draw from norm(max(0, p_n - q_n)) (rejection) or p_nd (bonus)
-      P2Job jb;
-      jb.b = b;
-      jb.n = n;
-      jb.mode = n < nd ? 0 : 1;
-      jb.mp = wf.rm[n];
-      jb.izp = 1.f / wf.rz[n];
-      jb.mq = n < nd ? wf.rm[nd + 1 + n] : 0.f;
-      jb.izq = n < nd ? 1.f / wf.rz[nd + 1 + n] : 0.f;
-      jb.c_hi = c.hi;
-      jb.c_lo = c.lo;
-      jb.pad[0] = jb.pad[1] = jb.pad[2] = 0;
-      jobs[b] = jb;
+    if (!greedy) {
+      // Every sampled request puts exactly one entry in the draw list -- its
+      // draw, or -1 when the request failed -- so the list's final length
+      // is the number of sampled requests, known from the start.
+      int entry = -1;
+      if (!err) {
+        // the draw from norm(max(0, p_n - q_n)) (rejection) or p_nd (bonus)
+        P2Job jb;
+        jb.b = b;
+        jb.n = n;
+        jb.mode = n < nd ? 0 : 1;
+        jb.mp = wf.rm[n];
+        jb.izp = rcp_fma(wf.rz[n]);  // Z >= 1
+        jb.mq = n < nd ? wf.rm[nd + 1 + n] : 0.f;
+        jb.izq = n < nd ? rcp_fma(wf.rz[nd + 1 + n]) : 0.f;
+        jb.c_hi = c.hi;
+        jb.c_lo = c.lo;
+        jb.pad[0] = jb.pad[1] = jb.pad[2] = 0;
+        jobs[b] = jb;
+        entry = b + 1;
+      }
+      fence_acq_rel_gpu();  // the job and the outputs before the entry
       const unsigned d = atomicAdd(&ws.hdr->draw_reserve, 1u);
-      st_release(ws.draws + d, b + 1);  // the job (and the outputs) before the entry
+      st_relaxed(ws.draws + d, entry);
     }
-    atomic_add_release(&ws.hdr->fin_count, 1u);  // the draw list entry before the count
   }
   __syncwarp();
 }

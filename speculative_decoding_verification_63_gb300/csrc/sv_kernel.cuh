@@ -6,16 +6,18 @@
 // always-ready consumers):
 //   warp  0      producer: moves chunks into the 4-stage ring with 1-D bulk
 //                copies: first the CTA's share of the main pass (chunks
-//                blockIdx.x, blockIdx.x + gridDim.x, ...), then draw-pass
-//                chunks claimed from a global counter; claim g is chunk
-//                g % ipr2 of the (g / ipr2)-th draw that request finalizes
-//                published in the global draw list (a claim waits for its
-//                draw, or lapses once every request is finalized and the
-//                list ends before it).  The 32 lanes work out the main-pass
-//                chunks 32 at a time (one each) and copy each chunk's
-//                metadata into the ring together; lane 0 waits for the slots
-//                and issues the copies.  With nothing left the producer ends
-//                the stream with one sentinel per consumer group.
+//                blockIdx.x, blockIdx.x + gridDim.x, ...), and draw-pass
+//                chunks claimed from a global counter as soon as their draws
+//                are published (ahead of the next main-pass chunk); claim g
+//                is chunk g % ipr2 of the (g / ipr2)-th entry of the global
+//                draw list, where every sampled request's finalize puts one
+//                entry (its draw, or -1 if it failed); claims beyond the
+//                number of sampled requests lapse.  The 32 lanes work out the main-pass
+//                chunks 32 at a time, each keeping its chunk's metadata in
+//                registers; each lane then puts its own chunk into the ring
+//                (16-byte stores, no loads) and issues the bulk copy.  With
+//                nothing left the producer ends the stream with one sentinel
+//                per consumer group.
 //   warp  1      bookkeeper: takes result slots in order, combines the 8
 //                per-warp partials of a chunk (max first, one rescale, a
 //                sum) or keeps the residual segment sums, stores them and
@@ -118,40 +120,32 @@ __device__ void producer_loop(const P& prob, Shared& sh, const PosTables& tab,
   const unsigned G = gridDim.x;
   int it = 0;                 // ring position
 
-  // Issue plan record k into the ring (all lanes): lane 0 waits for the
-  // slot, the lanes copy the record word by word, lane 0 publishes it and
-  // starts the bulk copies.
-  auto issue = [&](int k) {
-    const int stage = it % kStages;
-    const int rs = it % kResSlots;
-    if (lane == 0) {
-      if (it >= kStages) wait_or_flag(sh, &sh.empty[stage], ((it / kStages) - 1) & 1, err);
-      if (it >= kResSlots) wait_or_flag(sh, &sh.res_free[rs], ((it / kResSlots) - 1) & 1, err);
+  // Put a planned chunk into the ring; executed by the one lane holding the
+  // record: wait for the slot, store the metadata (16-byte stores, no loads),
+  // publish it and start the bulk copies.
+  auto issue_own = [&](const PlanRec& rec, int at) {
+    const int stage = at % kStages;
+    const int rs = at % kResSlots;
+    if (at >= kStages) wait_or_flag(sh, &sh.empty[stage], ((at / kStages) - 1) & 1, err);
+    if (at >= kResSlots) wait_or_flag(sh, &sh.res_free[rs], ((at / kResSlots) - 1) & 1, err);
+    uint4* dm = reinterpret_cast<uint4*>(&sh.meta[stage]);
+#pragma unroll
+    for (int q = 0; q < kStageWords; ++q) dm[q] = rec.v[q];
+    uint4* dr = reinterpret_cast<uint4*>(&sh.res_meta[rs]);
+#pragma unroll
+    for (int q = 0; q < kResWords16; ++q) dr[q] = rec.v[kStageWords + q];
+    mbar_arrive(&sh.res_done[rs]);
+    const StageMeta& m = rec.s.m;
+    if (prob.bulk) {
+      // one or two row pieces of n_el elements: [0, half) and [half, 2 half)
+      const uint32_t bytes = static_cast<uint32_t>(m.n_el * prob.es);
+      unsigned char* dst = stages + static_cast<size_t>(stage) * kChunkBytes;
+      mbar_arrive_expect_tx(&sh.full[stage], m.src2 ? 2u * bytes : bytes);
+      bulk_copy_g2s(dst, m.src, bytes, &sh.full[stage]);
+      if (m.src2) bulk_copy_g2s(dst + kChunkBytes / 2, m.src2, bytes, &sh.full[stage]);
+    } else {
+      mbar_arrive(&sh.full[stage]);
     }
-    __syncwarp();
-    if (lane < kMetaWords)
-      reinterpret_cast<int*>(&sh.meta[stage])[lane] = reinterpret_cast<const int*>(&sh.plan_m[k])[lane];
-    else if (lane < kMetaWords + kResWords)
-      reinterpret_cast<int*>(&sh.res_meta[rs])[lane - kMetaWords] =
-          reinterpret_cast<const int*>(&sh.plan_r[k])[lane - kMetaWords];
-    __syncwarp();  // every lane's words before lane 0's arrivals
-    if (lane == 0) {
-      const StageMeta& m = sh.plan_m[k];
-      mbar_arrive(&sh.res_done[rs]);
-      if (prob.bulk) {
-        // one or two row pieces of n_el elements: [0, half) and [half, 2 half)
-        const uint32_t bytes = static_cast<uint32_t>(m.n_el * prob.es);
-        const char* src2 = m.src2;
-        unsigned char* dst = stages + static_cast<size_t>(stage) * kChunkBytes;
-        mbar_arrive_expect_tx(&sh.full[stage], src2 ? 2u * bytes : bytes);
-        bulk_copy_g2s(dst, m.src, bytes, &sh.full[stage]);
-        if (src2) bulk_copy_g2s(dst + kChunkBytes / 2, src2, bytes, &sh.full[stage]);
-      } else {
-        mbar_arrive(&sh.full[stage]);
-      }
-    }
-    __syncwarp();
-    ++it;
   };
 
   // Draw-pass claims run alongside the main pass (lane 0): a claim is taken
@@ -159,13 +153,16 @@ __device__ void producer_loop(const P& prob, Shared& sh, const PosTables& tab,
   // advances one step (read the claim, poll the draw list, fetch the job,
   // plan the chunk); a planned draw chunk goes into the ring ahead of the
   // next main-pass chunk and the next claim is taken.  Claim g is chunk
-  // g % ipr2 of the (g / ipr2)-th published draw; claims beyond the number
-  // of sampled requests lapse at once.
+  // g % ipr2 of the (g / ipr2)-th entry of the draw list.  Every sampled
+  // request puts exactly one entry there (-1 if it failed), so claims beyond
+  // the number of sampled requests lapse at once and every other claim's
+  // entry is bound to appear.
   enum { D_NONE, D_CLAIMED, D_POLL, D_JOB };
   int dstate = D_NONE;
   unsigned dclaim = 0;
   int poll = 0;
   P2Job job{};
+  PlanRec drec;
   const unsigned cap = P::kHasDraws ? static_cast<unsigned>(sh.n_draw_cap) : 0u;
   if (lane == 0 && cap > 0) {
     dclaim = atomicAdd(&hdr->work_counter, 1u);
@@ -183,15 +180,21 @@ __device__ void producer_loop(const P& prob, Shared& sh, const PosTables& tab,
         dstate = D_POLL;
       } else if (dstate == D_POLL) {
         if (poll > 0) {
-          fence_acq_rel_gpu();  // the job, published before the entry
-          job = prob.load_job(poll - 1);
+          // the entry is there: read it again with acquire (the job was
+          // published before it), then fetch the job
+          const int e = ld_acquire(prob.ws.draws + d);
+          job = prob.load_job(e - 1);
           dstate = D_JOB;
+        } else if (poll < 0) {
+          // a request that failed: its draw has no chunks, take a new claim
+          dclaim = atomicAdd(&hdr->work_counter, 1u);
+          dstate = D_CLAIMED;
         } else {
           poll = ld_relaxed(prob.ws.draws + d);
         }
       } else if (dstate == D_JOB) {
-        StageMeta& mt = sh.plan_m[kDrawSlot];
-        ResMeta& rm = sh.plan_r[kDrawSlot];
+        StageMeta& mt = drec.s.m;
+        ResMeta& rm = drec.s.r;
         mt.item = 0x7fffffff;
         mt.pos = -1;
         mt.src2 = nullptr;
@@ -209,13 +212,15 @@ __device__ void producer_loop(const P& prob, Shared& sh, const PosTables& tab,
   };
 
   // Main pass: this CTA's share (chunks blockIdx.x + j G), worked out 32 at
-  // a time, one chunk per lane, then issued in order.
+  // a time, one chunk per lane and held in that lane's registers, then
+  // issued in order, each by its own lane.
   for (unsigned base = blockIdx.x; base < n_items; base += 32u * G) {
     const int cnt = static_cast<int>(min(32u, (n_items - base + G - 1u) / G));
+    PlanRec rec;
     if (lane < cnt) {
       const unsigned item = base + static_cast<unsigned>(lane) * G;
-      StageMeta& mt = sh.plan_m[lane];
-      ResMeta& rm = sh.plan_r[lane];
+      StageMeta& mt = rec.s.m;
+      ResMeta& rm = rec.s.r;
       const int row = static_cast<int>(item / prob.ipr);
       const int chunk = static_cast<int>(item % prob.ipr);
       const int pos = find_pos(tab.rstart, n_pos, row, -1);
@@ -231,66 +236,54 @@ __device__ void producer_loop(const P& prob, Shared& sh, const PosTables& tab,
       rm.c_hi = mt.c_hi;
       rm.c_lo = mt.c_lo;
     }
-    __syncwarp();
     for (int k = 0; k < cnt; ++k) {
       int have_draw = 0;
       if (lane == 0 && dstate != D_NONE) have_draw = draw_step() ? 1 : 0;
-      if (__shfl_sync(0xffffffffu, have_draw, 0)) issue(kDrawSlot);
-      issue(k);
+      have_draw = __shfl_sync(0xffffffffu, have_draw, 0);
+      if (have_draw) {
+        if (lane == 0) issue_own(drec, it);
+        ++it;
+      }
+      if (lane == k) issue_own(rec, it);
+      ++it;
     }
+    __syncwarp();
   }
 
   if constexpr (P::kHasDraws) {
     // The rest of the draw pass: lane 0 runs the claim machine until a chunk
-    // is planned, or the claim lapses (beyond the sampled requests, or every
-    // request finalized and the list shorter than its draw).
-    for (;;) {
-      int have = 0;
-      if (lane == 0) {
-        uint64_t t0 = 0;
-        unsigned backoff = 64;
-        while (dstate != D_NONE) {
-          if (draw_step()) {
-            have = 1;
+    // is planned or the claim lapses (beyond the sampled requests).
+    if (lane == 0) {
+      uint64_t t0 = 0;
+      unsigned backoff = 64;
+      while (dstate != D_NONE) {
+        if (draw_step()) {
+          issue_own(drec, it);
+          ++it;
+          t0 = 0;
+          backoff = 64;
+          continue;
+        }
+        if (dstate == D_POLL && poll == 0) {
+          const uint64_t now = globaltimer_ns();
+          if (t0 == 0) t0 = now;
+          if (now - t0 > wait_limit(sh)) {
+            flag_timeout(sh, err);
+            dstate = D_NONE;
             break;
           }
-          if (dstate == D_POLL && poll <= 0) {
-            const unsigned d = dclaim / static_cast<unsigned>(prob.ipr2);
-            if (ld_acquire(&hdr->fin_count) == static_cast<unsigned>(prob.n_req) &&
-                ld_relaxed(&hdr->draw_reserve) <= d) {
-              dstate = D_NONE;  // the list is final and ends before d
-              break;
-            }
-            const uint64_t now = globaltimer_ns();
-            if (t0 == 0) t0 = now;
-            if (now - t0 > wait_limit(sh)) {
-              flag_timeout(sh, err);
-              dstate = D_NONE;
-              break;
-            }
-            __nanosleep(backoff);
-            backoff = min(backoff * 2u, 512u);
-          }
+          __nanosleep(backoff);
+          backoff = min(backoff * 2u, 512u);
         }
       }
-      if (!__shfl_sync(0xffffffffu, have, 0)) break;
-      issue(kDrawSlot);
     }
+    it = __shfl_sync(0xffffffffu, it, 0);
   }
 
   // end of stream: one sentinel per consumer group (the bookkeeper stops at
   // the first)
-  for (int k = 0; k < kGroups; ++k) {
-    if (lane == 0) {
-      StageMeta& mt = sh.plan_m[0];
-      ResMeta& rm = sh.plan_r[0];
-      mt.item = -1;
-      mt.n_el = 0;
-      mt.src2 = nullptr;
-      rm.item = -1;
-    }
-    __syncwarp();
-    if (lane == 0) {
+  if (lane == 0) {
+    for (int k = 0; k < kGroups; ++k, ++it) {
       const int stage = it % kStages;
       const int rs = it % kResSlots;
       if (it >= kStages) wait_or_flag(sh, &sh.empty[stage], ((it / kStages) - 1) & 1, err);
@@ -300,9 +293,8 @@ __device__ void producer_loop(const P& prob, Shared& sh, const PosTables& tab,
       mbar_arrive(&sh.res_done[rs]);
       mbar_arrive(&sh.full[stage]);
     }
-    __syncwarp();
-    ++it;
   }
+  __syncwarp();
 }
 
 template <class P>
@@ -420,7 +412,7 @@ __device__ void ticketer_loop(const P& prob, Shared& sh) {
     __threadfence_block();  // the entries (and the bookkeeper's stores) before reading them
     const int nb = static_cast<int>(min(tail - head, 32u));
     const int4 e = lane < nb ? sh.bq[(head + lane) % kBqCap] : make_int4(0, 0, 0, 0);
-    __threadfence();  // the partials -> GPU scope before the tickets
+    fence_acq_rel_gpu();  // the partials (stored by the bookkeeper) -> GPU scope before the tickets
     bool done = false;
     if (lane < nb) {
       const unsigned old = atomic_add_acq_rel(&prob.ws.tickets[e.x], 1u);
@@ -428,7 +420,6 @@ __device__ void ticketer_loop(const P& prob, Shared& sh) {
     }
     const unsigned dmask = __ballot_sync(0xffffffffu, done);
     if (dmask) {
-      __threadfence();  // every partial of the completed entries is visible
       const unsigned ft = sh.fin_tail;
       // room: wait (bounded) while the list is full
       const unsigned need_room = ft + __popc(dmask);
@@ -618,7 +609,6 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const P prob) {
       hdr->work_counter = 0u;
       hdr->done_ctas = 0u;
       hdr->draw_reserve = 0u;
-      hdr->fin_count = 0u;
       __threadfence();
     }
   }

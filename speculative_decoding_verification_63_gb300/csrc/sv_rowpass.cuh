@@ -61,16 +61,14 @@ static_assert(kSpwF32 >= 1 && kSpwBf16 <= 4, "draw-pass segments per warp");
 enum RowKind : int { KIND_ARGMAX = 0, KIND_SOFTMAX = 1, KIND_TOPK = 2, KIND_RESID_PASS = 3 };
 
 constexpr int kFinResid = 0x40000000;  // finalize-list flag: a residual draw (request id below)
-constexpr int kDrawSlot = 32;                // producer plan entry of a draw-pass chunk
 constexpr int kDrawTicketBase = 1024;  // draw tickets follow the request tickets (SV_MAX_B)
 
 struct WsHeader {
   unsigned int work_counter;  // chunks claimed: main pass, then draw pass
   unsigned int done_ctas;
   int error;
-  unsigned int draw_reserve;  // draws published so far (entries of the draw list)
-  unsigned int fin_count;     // requests whose finalize has run (or that failed up front)
-  unsigned int pad[3];
+  unsigned int draw_reserve;  // entries of the draw list reserved so far
+  unsigned int pad[4];
 };
 
 // Device view of the caller's workspace.
@@ -108,7 +106,7 @@ struct StageMeta {
 };
 
 // What the bookkeeper needs about a result slot.
-struct ResMeta {
+struct __align__(16) ResMeta {
   int item;      // -1: no more work
   int kind;
   int slot;      // where the chunk's partial(s) go
@@ -118,10 +116,18 @@ struct ResMeta {
   float c_hi, c_lo;
 };
 
-static_assert(sizeof(StageMeta) % 4 == 0 && sizeof(ResMeta) == 32, "meta copied by words");
-constexpr int kMetaWords = sizeof(StageMeta) / 4;
-constexpr int kResWords = sizeof(ResMeta) / 4;
-static_assert(kMetaWords + kResWords <= 32, "one word per producer lane");
+// A planned chunk as the producer lane that planned it holds it: the stage
+// and result metadata, stored into the ring with 16-byte stores.
+union PlanRec {
+  struct {
+    StageMeta m;
+    ResMeta r;
+  } s;
+  uint4 v[(sizeof(StageMeta) + sizeof(ResMeta)) / 16];
+};
+static_assert(sizeof(StageMeta) % 16 == 0 && sizeof(ResMeta) == 32, "metadata in 16-byte words");
+constexpr int kStageWords = sizeof(StageMeta) / 16;
+constexpr int kResWords16 = sizeof(ResMeta) / 16;
 
 struct FinScratch {
   double dsum[kFinWarps];
@@ -152,8 +158,6 @@ struct __align__(16) Shared {
   uint64_t res_free[kResSlots];  // bookkeeper -> producer: slot consumed
   StageMeta meta[kStages];
   ResMeta res_meta[kResSlots];
-  StageMeta plan_m[33];         // the producer warp's next chunks, worked out together;
-  ResMeta plan_r[33];           // entry kDrawSlot: the next draw-pass chunk
   float4 res_part[kResSlots][kGroupWarps];
   int4 bq[kBqCap];             // booked chunks: ticket, count that completes it, finalize code
   unsigned bq_tail;            // entries published (bookkeeper only)
