@@ -115,8 +115,21 @@ sv_status launch(const P& prob, int grid, cudaStream_t stream) {
   if (cudaFuncSetAttribute(verify_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return SV_ECUDA;
-  verify_kernel<P><<<grid, kThreads, smem, stream>>>(prob);
-  const cudaError_t e = cudaGetLastError();
+  // programmatic stream serialisation: the kernel waits for the preceding
+  // work itself (griddepcontrol.wait), so its launch may overlap that work's
+  // tail
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, verify_kernel<P>, prob);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
     return SV_EUNSUPPORTED;
   return e == cudaSuccess ? SV_OK : SV_ECUDA;

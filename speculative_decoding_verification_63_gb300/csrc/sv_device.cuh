@@ -98,6 +98,17 @@ __device__ __forceinline__ void bulk_copy_g2s(void* smem_dst, const void* gmem_s
       : "memory");
 }
 
+// Programmatic dependent launch.  wait: block until the grids this launch
+// depends on have completed and their memory operations are visible.
+// launch_dependents: let the next dependent grid begin launching; it still
+// waits for this grid's completion before it touches memory.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Named barrier over the first `count` threads of the block.
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

@@ -543,6 +543,12 @@ __device__ void finalizer_loop(const P& prob, Shared& sh, const PosTables& tab) 
 template <class P>
 __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const P prob) {
   extern __shared__ __align__(1024) unsigned char smem_dyn[];
+  // Launched with programmatic stream serialisation: wait for the previous
+  // work on the stream (which may have produced the inputs, and used the
+  // same workspace) before touching global memory, and let the next launch
+  // start filling SMs as this one drains.
+  grid_dependency_wait();
+  grid_launch_dependents();
   // 128-byte aligned base (the launch adds 128 bytes of slack)
   unsigned char* smem_raw = smem_dyn + ((128u - (smem_u32(smem_dyn) & 127u)) & 127u);
   unsigned char* stages = smem_raw;

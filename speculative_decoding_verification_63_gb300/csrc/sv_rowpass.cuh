@@ -306,20 +306,30 @@ __device__ __forceinline__ void reduce_chunk_bf16(const StageMeta& mt, const uin
     }
     ms = MS{m, s};
   } else {
+    // lowest index of m: the first vector (ascending) whose maximum is m,
+    // then the first of its eight elements equal to m
     int idx = 0x7fffffff;
     if (m == m) {
+      int kk = -1;
 #pragma unroll
-      for (int k = 0; k < kVecPerThread; ++k) {
+      for (int k = kVecPerThread - 1; k >= 0; --k) {
         const int v = ctid + k * kGroupThreads;
-        const uint32_t w[4] = {r[k].x, r[k].y, r[k].z, r[k].w};
-        int cand = 0x7fffffff;
+        const float f = fmaxf(bf16lo(mk[k]), bf16hi(mk[k]));
+        if (v < nvec && f == m) kk = k;
+      }
+      if (kk >= 0) {
+        uint4 rv = r[0];
+#pragma unroll
+        for (int k = 1; k < kVecPerThread; ++k)
+          if (kk == k) rv = r[k];
+        const uint32_t w[4] = {rv.x, rv.y, rv.z, rv.w};
+        int j = 7;
 #pragma unroll
         for (int h = 3; h >= 0; --h) {  // descending, so the lowest match wins
-          const int e = mt.el_base + v * 8 + 2 * h;
-          if (bf16hi(w[h]) == m) cand = e + 1;
-          if (bf16lo(w[h]) == m) cand = e;
+          if (bf16hi(w[h]) == m) j = 2 * h + 1;
+          if (bf16lo(w[h]) == m) j = 2 * h;
         }
-        if (v < nvec) idx = min(idx, cand);
+        idx = mt.el_base + (ctid + kk * kGroupThreads) * 8 + j;
       }
     }
     vi = VI{m, idx};
@@ -403,10 +413,12 @@ struct ResidParams {
 // explicitly rounded intrinsic, so the chunk pass and the final rescan
 // produce the same bits.
 __device__ __forceinline__ float resid_weight(float xp, float xq, const ResidParams& r) {
-  const float dp = fmaxf(__fsub_rn(xp, r.mp), -1.0e30f);
+  // mp and mq are finite (a row whose maximum is not is an error and gets
+  // no draw), so x = -inf gives d = -inf and a weight of 0
+  const float dp = __fsub_rn(xp, r.mp);
   const float ep = fast_exp2(__fmaf_rn(dp, r.c.hi, __fmul_rn(dp, r.c.lo)));
   if (r.mode != 0) return ep;
-  const float dq = fmaxf(__fsub_rn(xq, r.mq), -1.0e30f);
+  const float dq = __fsub_rn(xq, r.mq);
   const float eq = fast_exp2(__fmaf_rn(dq, r.c.hi, __fmul_rn(dq, r.c.lo)));
   return fmaxf(__fsub_rn(__fmul_rn(ep, r.izp), __fmul_rn(eq, r.izq)), 0.f);
 }
