@@ -79,7 +79,7 @@ typedef enum {
 #define SV_MAX_K 32        /* drafts per chain */
 #define SV_MAX_B 1024      /* requests per call */
 #define SV_MAX_V (1 << 20) /* vocabulary entries */
-#define SV_MAX_TOPK 256    /* top-k filter size */
+#define SV_MAX_TOPK 64     /* top-k filter size */
 #define SV_MAX_TREE_NODES 64 /* nodes per tree (N) and draft rows (M) */
 #define SV_MAX_TREE_B 1024  /* requests per tree call */
 
@@ -102,6 +102,12 @@ typedef enum {
  * at (b*K + i) * draft_row_stride.  Rows whose byte address and stride are
  * multiples of 16 (bf16: V a multiple of 8) take the bulk-copy path; others
  * a slower direct path.
+ *
+ * With a top_k array and max_top_k > 0 the call launches two kernels on the
+ * stream: a pass that reduces every filtered row to its top-k (logit, id)
+ * list and (max, sum of exp) in the workspace, then the verification kernel,
+ * which reads no filtered row itself and finalizes filtered requests from
+ * those lists.  Otherwise one kernel.
  */
 typedef struct {
   int32_t B, K, V;
@@ -114,9 +120,12 @@ typedef struct {
   const int32_t* draft_tokens; /* [B][K] */
   const int32_t* num_drafts;   /* [B] in [0, K], or NULL (= K) */
   const float* temperature;    /* [B]; 0 = greedy; < 0 or NaN -> SV_DERR_ARG */
-  const int32_t* top_k;        /* [B] or NULL; 0 = no filter; must be
-                                  <= max_top_k unless >= V */
-  int32_t max_top_k;           /* host-known bound on top_k (0 = none) */
+  const int32_t* top_k;        /* [B] or NULL; 0 or >= V = no filter; a
+                                  filter keeps the top_k largest logits of p
+                                  and of q (ties: lower id first) and must be
+                                  <= max_top_k (else SV_DERR_ARG) */
+  int32_t max_top_k;           /* host-known bound on top_k (0 = none);
+                                  sizes the workspace's top-k lists */
   const float* uniforms;       /* [B][K+1] in [0,1): [0..K-1] accept tests,
                                   [K] the residual / bonus draw */
   int32_t* out_tokens;         /* [B][K+1]: accepted drafts then the emitted

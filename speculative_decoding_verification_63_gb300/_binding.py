@@ -19,7 +19,7 @@ SV_BF16, SV_FP32 = 0, 1
 SV_TREE_MSS = 0
 SV_DERR_TOKEN, SV_DERR_NONFINITE, SV_DERR_MASS = 0x01, 0x02, 0x04
 SV_DERR_TREE, SV_DERR_TIMEOUT, SV_DERR_ARG = 0x08, 0x10, 0x20
-SV_MAX_K, SV_MAX_B, SV_MAX_V, SV_MAX_TOPK = 32, 1024, 1 << 20, 256
+SV_MAX_K, SV_MAX_B, SV_MAX_V, SV_MAX_TOPK = 32, 1024, 1 << 20, 64
 SV_MAX_TREE_NODES, SV_MAX_TREE_B = 64, 1024
 
 # every symbol include/specverify.h declares

@@ -7,6 +7,7 @@
 
 #include "specverify.h"
 #include "sv_chain.cuh"
+#include "sv_topk.cuh"
 #include "sv_tree.cuh"
 
 namespace {
@@ -17,24 +18,30 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 struct Layout {
-  size_t tickets, draws, jobs, partials, segsums, scratch, total;
+  size_t tickets, draws, jobs, topk_done, partials, segsums, scratch, total;
 };
 
+// top-k pass: one counter per row (b, i) of a chain call
+constexpr size_t kTopkRows = static_cast<size_t>(SV_MAX_B) * (2 * SV_MAX_K + 1);
+
 static_assert(kDrawTicketBase == SV_MAX_B, "draw tickets follow the request tickets");
+static_assert(kTkMaxSegs * SV_MAX_TOPK <= kTkCap, "a row's segment lists fit one warp's buffer");
+static_assert(2 * SV_MAX_K + 1 <= 96, "top-k finalize: row statistics in three lanes' strides");
 static_assert(SV_MAX_V / kRSeg <= kMaxPages * kPageSeg && 2 * kMaxPages <= kMaxRowsPerReq,
               "draw finalize pages");
 
-// The header, the tickets (requests, then their draws) and the draw list
-// sit at fixed offsets with a fixed capacity (SV_MAX_B), so the region that
-// every call leaves zeroed is the same for all problem sizes: one
-// initialised workspace serves chain and tree calls of any shape, one call
-// at a time.
+// The header, the tickets (requests, then their draws), the draw list and
+// the top-k pass's row counters sit at fixed offsets with a fixed capacity
+// (SV_MAX_B requests), so the region that every call leaves zeroed is the
+// same for all problem sizes: one initialised workspace serves chain and
+// tree calls of any shape, one call at a time.
 Layout layout_for(int64_t partial_slots, int64_t segsum_floats, int64_t scratch_floats) {
   Layout L;
   L.tickets = align_up(sizeof(WsHeader));
   L.draws = align_up(L.tickets + sizeof(unsigned int) * 2 * static_cast<size_t>(SV_MAX_B));
   L.jobs = align_up(L.draws + sizeof(int) * static_cast<size_t>(SV_MAX_B));
-  L.partials = align_up(L.jobs + sizeof(P2Job) * static_cast<size_t>(SV_MAX_B));
+  L.topk_done = align_up(L.jobs + sizeof(P2Job) * static_cast<size_t>(SV_MAX_B));
+  L.partials = align_up(L.topk_done + sizeof(unsigned int) * kTopkRows);
   L.segsums = align_up(L.partials + sizeof(float2) * static_cast<size_t>(partial_slots));
   L.scratch = align_up(L.segsums + sizeof(float) * static_cast<size_t>(segsum_floats));
   L.total = align_up(L.scratch + sizeof(float) * static_cast<size_t>(scratch_floats));
@@ -58,12 +65,36 @@ int es_of(sv_dtype d) { return d == SV_BF16 ? 2 : 4; }
 int chunk_el_of(sv_dtype d) { return kChunkBytes / es_of(d); }
 int resid_chunk_el_of(sv_dtype d) { return kChunkBytes / 2 / es_of(d); }
 
+// Top-k pass: segments per row and their length, and the scratch it uses
+// (byte offsets within the scratch region): per row its list and (m, Z),
+// per segment its list and count.
+struct TopkLayout {
+  int n_seg = 0, seg_len = 0;
+  size_t lists = 0, mz = 0, seg_lists = 0, seg_count = 0, bytes = 0;
+};
+TopkLayout topk_layout(int64_t B, int64_t K, int64_t V, int64_t max_top_k) {
+  TopkLayout T;
+  if (max_top_k <= 0) return T;
+  const int64_t s0 = std::min<int64_t>(kTkMaxSegs, std::max<int64_t>(1, (V + kTkMinSeg - 1) / kTkMinSeg));
+  const int64_t per = (V + s0 - 1) / s0;
+  T.seg_len = static_cast<int>((per + kTkStep - 1) / kTkStep * kTkStep);
+  T.n_seg = static_cast<int>((V + T.seg_len - 1) / T.seg_len);  // every segment non-empty
+  const size_t rows = static_cast<size_t>(B) * (2 * K + 1);
+  T.lists = 0;
+  T.mz = align_up(T.lists + sizeof(float2) * rows * max_top_k);
+  T.seg_lists = align_up(T.mz + sizeof(float2) * rows);
+  T.seg_count = align_up(T.seg_lists + sizeof(float2) * rows * T.n_seg * max_top_k);
+  T.bytes = align_up(T.seg_count + sizeof(int) * rows * T.n_seg);
+  return T;
+}
+
 // Chain calls: per-row chunk partials for the main pass, per-request
-// segment sums for the draw pass.
-Layout chain_layout(int64_t B, int64_t K, int64_t V, sv_dtype dtype) {
+// segment sums for the draw pass, and the top-k pass's scratch.
+Layout chain_layout(int64_t B, int64_t K, int64_t V, sv_dtype dtype, int64_t max_top_k) {
   const int64_t ipr = (V + chunk_el_of(dtype) - 1) / chunk_el_of(dtype);
   const int64_t ipr2 = (V + resid_chunk_el_of(dtype) - 1) / resid_chunk_el_of(dtype);
-  return layout_for(B * (2 * K + 1) * ipr, B * ipr2 * (resid_chunk_el_of(dtype) / kRSeg), 0);
+  return layout_for(B * (2 * K + 1) * ipr, B * ipr2 * (resid_chunk_el_of(dtype) / kRSeg),
+                    static_cast<int64_t>(topk_layout(B, K, V, max_top_k).bytes / sizeof(float)));
 }
 
 Layout tree_layout(int64_t B, int64_t N, int64_t M, int64_t V, sv_dtype dtype) {
@@ -140,6 +171,33 @@ bool bulk_ok(const void* base, int64_t stride_bytes, int64_t row_bytes) {
          (stride_bytes & 15) == 0 && (row_bytes & 15) == 0;
 }
 
+// rows start on 16-byte boundaries (16-byte loads; a row's ragged end is
+// read element by element)
+bool aligned16(const void* base, int64_t stride_bytes) {
+  return base != nullptr && (reinterpret_cast<uintptr_t>(base) & 15) == 0 &&
+         (stride_bytes & 15) == 0;
+}
+
+sv_status launch_topk(const TopkPass& t, int grid, cudaStream_t stream) {
+  // programmatic stream serialisation, as for the persistent kernel: the
+  // pass waits for the preceding work itself
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(std::max(grid, 1)));
+  cfg.blockDim = dim3(kTkThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, topk_kernel, t);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
+    return SV_EUNSUPPORTED;
+  return e == cudaSuccess ? SV_OK : SV_ECUDA;
+}
+
 __global__ void wait_selftest_kernel(WsHeader* hdr, uint64_t limit_ns) {
   __shared__ uint64_t bar;
   if (threadIdx.x == 0) {
@@ -213,7 +271,7 @@ size_t sv_chain_workspace_bytes(int32_t B, int32_t K, int32_t V, sv_dtype dtype,
   if (B < 0 || B > SV_MAX_B || K < 0 || K > SV_MAX_K || V < 1 || V > SV_MAX_V ||
       (dtype != SV_BF16 && dtype != SV_FP32) || max_top_k < 0 || max_top_k > SV_MAX_TOPK)
     return 0;
-  return chain_layout(B, K, V, dtype).total;
+  return chain_layout(B, K, V, dtype, max_top_k).total;
 }
 
 size_t sv_tree_workspace_bytes(int32_t B, int32_t N, int32_t M, int32_t V, sv_dtype dtype,
@@ -258,7 +316,8 @@ sv_status sv_verify_chain(const sv_chain_args* a, void* workspace, size_t ws_byt
   const int es = es_of(a->dtype);
   const int chunk_el = chunk_el_of(a->dtype);
   const int ipr = (a->V + chunk_el - 1) / chunk_el;
-  const Layout L = chain_layout(a->B, a->K, a->V, a->dtype);
+  const Layout L = chain_layout(a->B, a->K, a->V, a->dtype, a->max_top_k);
+  const TopkLayout TL = topk_layout(a->B, a->K, a->V, a->max_top_k);
 
   ChainProblem p;
   p.n_req = a->B;
@@ -289,10 +348,46 @@ sv_status sv_verify_chain(const sv_chain_args* a, void* workspace, size_t ws_byt
   p.jobs = static_cast<P2Job*>(p.ws.jobs);
   p.chunk2 = resid_chunk_el_of(a->dtype);
   p.ipr2 = (a->V + p.chunk2 - 1) / p.chunk2;
+  char* scratch = reinterpret_cast<char*>(p.ws.scratch);
+  p.topk_lists = reinterpret_cast<const float2*>(scratch + TL.lists);
+  p.topk_mz = reinterpret_cast<const float2*>(scratch + TL.mz);
 
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (a->top_k != nullptr && a->max_top_k > 0) {
+    // the top-k lists first; the persistent kernel finalizes top-k
+    // requests from them
+    TopkPass t;
+    t.n_req = a->B;
+    t.K = a->K;
+    t.V = a->V;
+    t.es = es;
+    t.max_topk = a->max_top_k;
+    t.n_seg = TL.n_seg;
+    t.seg_len = TL.seg_len;
+    t.has_draft = a->draft_logits != nullptr;
+    t.target = p.target;
+    t.t_stride = p.t_stride;
+    t.draft = p.draft;
+    t.d_stride = p.d_stride;
+    t.vec = aligned16(a->target_logits, p.t_stride) &&
+            (a->draft_logits == nullptr || aligned16(a->draft_logits, p.d_stride));
+    t.num_drafts = a->num_drafts;
+    t.temperature = a->temperature;
+    t.top_k = a->top_k;
+    t.seg_lists = reinterpret_cast<float2*>(scratch + TL.seg_lists);
+    t.seg_count = reinterpret_cast<int*>(scratch + TL.seg_count);
+    t.lists = reinterpret_cast<float2*>(scratch + TL.lists);
+    t.mz = reinterpret_cast<float2*>(scratch + TL.mz);
+    t.row_done = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + L.topk_done);
+    const int64_t items = static_cast<int64_t>(a->B) * (2 * a->K + 1) * TL.n_seg;
+    const int64_t ctas = std::min<int64_t>((items + kTkWarps - 1) / kTkWarps,
+                                             static_cast<int64_t>(kTkCtasPerSm) * dev.sms);
+    const sv_status ts = launch_topk(t, static_cast<int>(ctas), st);
+    if (ts != SV_OK) return ts;
+  }
   const int64_t items_max = static_cast<int64_t>(a->B) * (2 * a->K + 1) * ipr;
   const int grid = static_cast<int>(std::min<int64_t>(std::max<int64_t>(items_max, 1), dev.sms));
-  return launch(p, grid, reinterpret_cast<cudaStream_t>(stream));
+  return launch(p, grid, st);
 }
 
 sv_status sv_verify_tree(const sv_tree_args* a, void* workspace, size_t ws_bytes,

@@ -34,6 +34,7 @@ struct ChainProblem {
   static constexpr int kAuxBytes = 0;
   static constexpr bool kWarpFinalize = true;
   static constexpr bool kHasDraws = true;
+  static constexpr bool kHasDirectFin = true;  // top-k requests: finalize only
   int n_req, K, V, es, ipr, chunk_el, max_topk;
   int ipr2, chunk2;  // draw pass: chunks per row pair, tokens per chunk
   bool bulk;
@@ -52,18 +53,15 @@ struct ChainProblem {
   float* p_at;
   float* q_at;
   P2Job* jobs;  // [SV_MAX_B] the draw of request b
+  const float2* topk_lists;  // [B (2K+1)][max_topk] top-k (logit, id) of row (b, i), token order
+  const float2* topk_mz;     // [B (2K+1)] (m, Z) over those logits
   Ws ws;
 
   // kind of request b, or -1 if its scalar arguments are invalid
   __device__ int classify(int b, int& nd) const {
     nd = num_drafts ? num_drafts[b] : K;
-    const float t = temperature[b];
-    const int tk = top_k ? top_k[b] : 0;
-    const bool filtered = tk > 0 && tk < V;
-    if (nd < 0 || nd > K || !(t >= 0.f) || tk < 0) return -1;
-    if (t == 0.f) return KIND_ARGMAX;
-    if ((draft == nullptr && nd > 0) || filtered) return -1;  // top-k: not yet supported
-    return KIND_SOFTMAX;
+    return chain_kind(nd, temperature[b], top_k ? top_k[b] : 0, K, V, max_topk,
+                      draft != nullptr);
   }
 
   __device__ void write_failed(int b, int flag) const {
@@ -79,7 +77,8 @@ struct ChainProblem {
 
   // Processing order: sampled requests first (their draw pass should overlap
   // the rest of the main pass), then greedy ones.  rows: greedy nd+1,
-  // sampled 2nd+1.
+  // sampled 2nd+1; top-k requests read no rows here (the top-k pass has
+  // reduced them to lists) and go straight to their finalize.
   __device__ void preamble(Shared& sh, PosTables& tab, int4* scan_tmp) const {
     const int per = (n_req + kThreads - 1) / kThreads;
     const int lo = min(static_cast<int>(threadIdx.x) * per, n_req);
@@ -92,7 +91,7 @@ struct ChainProblem {
         cnt.z += 1;
         continue;
       }
-      const int rows = kind == KIND_ARGMAX ? nd + 1 : 2 * nd + 1;
+      const int rows = kind == KIND_ARGMAX ? nd + 1 : (kind == KIND_TOPK ? 0 : 2 * nd + 1);
       if (kind == KIND_SOFTMAX) {
         cnt.x += 1;
         cnt.y += rows;
@@ -114,7 +113,7 @@ struct ChainProblem {
         tab.rstart[pos] = hrow;
         hrow += rows;
       } else {
-        rows = kind < 0 ? 0 : (kind == KIND_ARGMAX ? nd + 1 : 2 * nd + 1);
+        rows = kind == KIND_ARGMAX ? nd + 1 : 0;
         pos = lpos++;
         tab.rstart[pos] = lrow;
         lrow += rows;
@@ -292,11 +291,17 @@ struct ChainProblem {
     return make_float4(r.x, r.y, 0.f, 0.f);
   }
 
+  // a request whose finalize needs no main-pass rows
+  __device__ bool direct_fin(const PosTables& tab, int pos) const {
+    return info_kind(tab.info[pos]) == KIND_TOPK;
+  }
   __device__ void finalize_warp(Shared& sh, const PosTables& tab, int code, int lane,
                                 WarpFin& wf) const {
     if (code & kFinResid) draw_finalize(code & ~kFinResid, lane, wf);
+    else if (info_kind(tab.info[code]) == KIND_TOPK) topk_finalize(tab, code, lane, wf);
     else request_finalize(sh, tab, code, lane, wf);
   }
+  __device__ void topk_finalize(const PosTables& tab, int pos, int lane, WarpFin& wf) const;
   __device__ void request_finalize(Shared& sh, const PosTables& tab, int pos, int lane,
                                    WarpFin& wf) const;
   __device__ void draw_finalize(int b, int lane, WarpFin& wf) const;
@@ -627,6 +632,193 @@ __device__ void ChainProblem::draw_finalize(int b, int lane, WarpFin& wf) const 
       record_error(&ws.hdr->error, 0x04);
     }
     ws.tickets[kDrawTicketBase + b] = 0u;
+  }
+  __syncwarp();
+}
+
+// Finalize of a top-k request from the top-k pass's lists: row (b, i) holds
+// the k largest logits of that row with their ids, in token order, and
+// (m, Z) over them.  p_i(x) = exp((l - m)/t) / Z for x in p_i's list and 0
+// otherwise (likewise q_i), so the accept tests look the drafts up in the
+// lists; the residual max(0, p_n - q_n), or p_nd for the bonus, is nonzero
+// only on p_n's list, which is already in token order for the inverse CDF.
+__device__ void ChainProblem::topk_finalize(const PosTables& tab, int pos, int lane,
+                                            WarpFin& wf) const {
+  const int info = tab.info[pos];
+  const int b = info_req(info), nd = info_extra(info);
+  const int r0 = b * (2 * K + 1);   // rows (b, 0 .. 2K): target 0..nd, draft nd+1 ..
+  const int nrows = 2 * nd + 1;
+  const Scale2 c{tab.scale[pos].x, tab.scale[pos].y};
+  const int k = top_k[b];
+  auto list_of = [&](int row) { return topk_lists + static_cast<size_t>(r0 + row) * max_topk; };
+
+  const int x = lane < nd ? tokens[static_cast<size_t>(b) * K + lane] : 0;
+  const float ui = lane < nd ? uniforms[static_cast<size_t>(b) * (K + 1) + lane] : 0.f;
+  const float uK = uniforms[static_cast<size_t>(b) * (K + 1) + K];
+  // row statistics (nrows <= 2 SV_MAX_K + 1 = 65: rows lane, lane + 32, lane + 64)
+  int err = 0;
+#pragma unroll
+  for (int t = 0; t < 3; ++t) {
+    const int j = lane + 32 * t;
+    if (j < nrows) {
+      const float2 v = topk_mz[r0 + j];
+      if (v.x != v.x) err |= 0x02;
+      else if (v.x == kNegInf || !(v.y > 0.f)) err |= 0x04;
+      wf.rm[j] = v.x;
+      wf.rz[j] = v.y;
+    }
+  }
+  // slot of x_i in p_i's list (ridx[2i]) and in q_i's (ridx[2i+1]), -1 if
+  // absent: every (list, slot) pair is checked by some lane, eight loads in
+  // flight at a time
+  for (int i = lane; i < 2 * nd; i += 32) wf.ridx[i] = -1;
+  __syncwarp();
+  const int total = 2 * nd * k;
+  for (int e0 = 0; e0 < total; e0 += 32 * 8) {
+    int idv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = e0 + u * 32 + lane;
+      idv[u] = -1;
+      if (e < total) {
+        const int which = e / (nd * k), rem = e % (nd * k), i = rem / k, slot = rem % k;
+        idv[u] = __float_as_int(list_of(which ? nd + 1 + i : i)[slot].y);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = e0 + u * 32 + lane;
+      if (e < total) {
+        const int which = e / (nd * k), rem = e % (nd * k), i = rem / k, slot = rem % k;
+        if (idv[u] >= 0 && idv[u] == tokens[static_cast<size_t>(b) * K + i])
+          wf.ridx[2 * i + which] = slot;
+      }
+    }
+  }
+  __syncwarp();
+
+  // accept tests (lane i = draft i), as in the unfiltered finalize
+  bool acc = false;
+  const double cd = static_cast<double>(c.hi) + static_cast<double>(c.lo);
+  if (lane < nd) {
+    if (x < 0 || x >= V) {
+      err |= 0x01;
+    } else {
+      const int sp = wf.ridx[2 * lane], sq = wf.ridx[2 * lane + 1];
+      const int jt = lane, jd = nd + 1 + lane;
+      double np = 0.0, nq = 0.0;
+      if (sp >= 0)
+        np = exp2_nonpos((static_cast<double>(list_of(jt)[sp].x) -
+                          static_cast<double>(wf.rm[jt])) * cd);
+      if (sq >= 0)
+        nq = exp2_nonpos((static_cast<double>(list_of(jd)[sq].x) -
+                          static_cast<double>(wf.rm[jd])) * cd);
+      const double zp = static_cast<double>(wf.rz[jt]), zq = static_cast<double>(wf.rz[jd]);
+      acc = static_cast<double>(ui) * nq * zp < np * zq;
+      if (!err) {
+        if (p_at) p_at[static_cast<size_t>(b) * K + lane] = static_cast<float>(np) * rcp_fma(wf.rz[jt]);
+        if (q_at) q_at[static_cast<size_t>(b) * K + lane] = static_cast<float>(nq) * rcp_fma(wf.rz[jd]);
+      }
+    }
+  }
+  err = __reduce_or_sync(0xffffffffu, err);
+  for (int i = lane; i < K; i += 32) {
+    if (err || i >= nd) {
+      if (p_at) p_at[static_cast<size_t>(b) * K + i] = __int_as_float(0x7fc00000);
+      if (q_at) q_at[static_cast<size_t>(b) * K + i] = __int_as_float(0x7fc00000);
+    }
+  }
+  const unsigned mask = __ballot_sync(0xffffffffu, acc);
+  int n = mask == 0xffffffffu ? 32 : __ffs(~mask) - 1;
+  n = min(n, nd);
+
+  // the draw over p_n's list: lane l holds slots 2l and 2l+1 (token order);
+  // for the residual, q_n's logit of the same token if it is in q_n's list
+  int token = -1;
+  if (!err) {
+    const int mode0 = n < nd ? 0 : 1;
+    const int jp = n, jq = nd + 1 + n;
+    float pv[2], xq[2];
+    int pid[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int slot = 2 * lane + t;
+      const float2 a = slot < k ? list_of(jp)[slot] : make_float2(kNegInf, __int_as_float(-1));
+      pv[t] = a.x;
+      pid[t] = __float_as_int(a.y);
+      xq[t] = kNegInf;
+    }
+    if (mode0 == 0) {
+      // q_n's list, slots lane and lane + 32, searched by every lane
+      float qv[2];
+      int qid[2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int slot = lane + 32 * t;
+        const float2 q = slot < k ? list_of(jq)[slot] : make_float2(kNegInf, __int_as_float(-1));
+        qv[t] = q.x;
+        qid[t] = __float_as_int(q.y);
+      }
+      for (int s2 = 0; s2 < 64; ++s2) {
+        const int src = s2 & 31, tt = s2 >> 5;
+        const int id2 = __shfl_sync(0xffffffffu, tt ? qid[1] : qid[0], src);
+        const float v2 = __shfl_sync(0xffffffffu, tt ? qv[1] : qv[0], src);
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          if (id2 >= 0 && id2 == pid[t]) xq[t] = v2;
+      }
+    }
+    const float mp = wf.rm[jp], izp = rcp_fma(wf.rz[jp]);
+    const float mq = mode0 == 0 ? wf.rm[jq] : 0.f, izq = mode0 == 0 ? rcp_fma(wf.rz[jq]) : 0.f;
+    for (int attempt = 0; attempt < 2 && token < 0; ++attempt) {
+      // attempt 1: a residual of zero mass (rounding only) draws from p_n
+      if (attempt == 1 && mode0 != 0) break;
+      const int mode = attempt == 0 ? mode0 : 1;
+      const ResidParams rp{mp, izp, mode == 0 ? mq : 0.f, mode == 0 ? izq : 0.f, c, mode};
+      float w[2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) w[t] = pid[t] >= 0 ? resid_weight(pv[t], xq[t], rp) : 0.f;
+      // float-pair running sums in token order
+      const DF incl = warp_incl_scan_df(df_add(df_add(DF{0.f, 0.f}, w[0]), w[1]), lane);
+      const DF S = df_shfl(incl, 31);
+      if (!(S.hi > 0.f)) continue;
+      const DF target = df_mul(uK, S);
+      DF excl = df_shfl(incl, lane > 0 ? lane - 1 : 0);
+      if (lane == 0) excl = DF{0.f, 0.f};
+      const DF e1 = df_add(excl, w[0]);
+      // the first slot (token order) whose running sum exceeds target
+      const bool h0 = w[0] > 0.f && df_lt(target, e1);
+      const bool h1 = !h0 && w[1] > 0.f && df_lt(target, df_add(e1, w[1]));
+      const unsigned hit = __ballot_sync(0xffffffffu, h0 || h1);
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        token = __shfl_sync(0xffffffffu, h0 ? pid[0] : pid[1], src);
+      } else {
+        // rounding left target at the end: the last slot with weight
+        const int lastp = w[1] > 0.f ? 1 : (w[0] > 0.f ? 0 : -1);
+        const unsigned anyp = __ballot_sync(0xffffffffu, lastp >= 0);
+        if (anyp) {
+          const int src = 31 - __clz(anyp);
+          token = __shfl_sync(0xffffffffu, lastp == 1 ? pid[1] : pid[0], src);
+        }
+      }
+    }
+    if (token < 0) err |= 0x04;
+  }
+
+  // outputs
+  for (int i = lane; i <= K; i += 32) {
+    int v = -1;
+    if (!err) {
+      if (i < n) v = tokens[static_cast<size_t>(b) * K + i];
+      else if (i == n) v = token;
+    }
+    out_tokens[static_cast<size_t>(b) * (K + 1) + i] = v;
+  }
+  if (lane == 0) {
+    out_len[b] = err ? 0 : n + 1;
+    accept_len[b] = err ? 0 : n;
+    if (err) record_error(&ws.hdr->error, err);
   }
   __syncwarp();
 }

@@ -267,6 +267,14 @@ __device__ __forceinline__ float warp_incl_scan(float x, int lane) {
   }
   return x;
 }
+__device__ __forceinline__ unsigned warp_incl_scan_u(unsigned x, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  return x;
+}
 __device__ __forceinline__ double warp_incl_scan_d(double x, int lane) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {

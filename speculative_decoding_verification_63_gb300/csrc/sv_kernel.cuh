@@ -62,6 +62,9 @@
 //   void finalize(Shared&, const PosTables&, int code, int ftid) const
 //                                          (!kWarpFinalize, all 4 warps)
 //   void last_cta_reset() const  (the last CTA to finish, after all others)
+//   static constexpr bool kHasDirectFin  some requests need no main-pass rows
+//   bool direct_fin(const PosTables&, int pos) const
+//        -> request at pos goes straight to the finalize list (kHasDirectFin)
 #pragma once
 
 #include "sv_rowpass.cuh"
@@ -377,14 +380,51 @@ __device__ void bookkeeper_loop(const P& prob, Shared& sh) {
   __syncwarp();
 }
 
-// The ticket warp: takes booked chunks in batches of up to 32 (lane i one
-// chunk), makes their partials visible GPU-wide, bumps their tickets and
-// puts each request or draw whose ticket completes on the finalize list.
-// The fence and the atomics' round trip happen here, off the result ring.
+// Append the codes of the lanes with `done` to the finalize list (ticket
+// warp only; all lanes call it): waits, bounded, while the list is full.
+__device__ __forceinline__ void fin_push(Shared& sh, bool done, int code, int lane, int* err) {
+  const unsigned dmask = __ballot_sync(0xffffffffu, done);
+  if (!dmask) return;
+  const unsigned ft = vload(sh.fin_tail);
+  const unsigned need_room = ft + __popc(dmask);
+  if (need_room - vload(sh.fin_claim) > static_cast<unsigned>(kFinCap)) {
+    const uint64_t t0 = globaltimer_ns();
+    while (need_room - vload(sh.fin_claim) > static_cast<unsigned>(kFinCap)) {
+      __nanosleep(200);
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (lane == 0) record_error(err, 0x10);
+        break;
+      }
+    }
+  }
+  if (done)
+    reinterpret_cast<volatile int*>(sh.fin_q)[(ft + __popc(dmask & ((1u << lane) - 1u))) %
+                                               kFinCap] = code;
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence_block();
+    *reinterpret_cast<volatile unsigned*>(&sh.fin_tail) = need_room;
+  }
+  __syncwarp();
+}
+
+// The ticket warp: first puts this CTA's share of the requests that need no
+// main-pass rows (positions blockIdx.x + j G) on the finalize list; then
+// takes booked chunks in batches of up to 32 (lane i one chunk), makes
+// their partials visible GPU-wide, bumps their tickets and puts each
+// request or draw whose ticket completes on the finalize list.  The fence
+// and the atomics' round trip happen here, off the result ring.
 template <class P>
-__device__ void ticketer_loop(const P& prob, Shared& sh) {
+__device__ void ticketer_loop(const P& prob, Shared& sh, const PosTables& tab) {
   int* err = &prob.ws.hdr->error;
   const int lane = threadIdx.x & 31;
+  if constexpr (P::kHasDirectFin) {
+    const int G = static_cast<int>(gridDim.x);
+    for (int p0 = static_cast<int>(blockIdx.x); p0 < sh.n_pos; p0 += 32 * G) {
+      const int p = p0 + lane * G;
+      fin_push(sh, p < sh.n_pos && prob.direct_fin(tab, p), p, lane, err);
+    }
+  }
   unsigned head = 0;
   uint64_t idle_since = 0;
   unsigned backoff = 32;
@@ -418,30 +458,7 @@ __device__ void ticketer_loop(const P& prob, Shared& sh) {
       const unsigned old = atomic_add_acq_rel(&prob.ws.tickets[e.x], 1u);
       done = old + 1u == static_cast<unsigned>(e.y);
     }
-    const unsigned dmask = __ballot_sync(0xffffffffu, done);
-    if (dmask) {
-      const unsigned ft = sh.fin_tail;
-      // room: wait (bounded) while the list is full
-      const unsigned need_room = ft + __popc(dmask);
-      if (need_room - vload(sh.fin_claim) > static_cast<unsigned>(kFinCap)) {
-        const uint64_t t0 = globaltimer_ns();
-        while (need_room - vload(sh.fin_claim) > static_cast<unsigned>(kFinCap)) {
-          __nanosleep(200);
-          if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            if (lane == 0) record_error(err, 0x10);
-            break;
-          }
-        }
-      }
-      if (done)
-        reinterpret_cast<volatile int*>(sh.fin_q)[(ft + __popc(dmask & ((1u << lane) - 1u))) %
-                                                   kFinCap] = e.z;
-      __syncwarp();
-      if (lane == 0) {
-        __threadfence_block();
-        *reinterpret_cast<volatile unsigned*>(&sh.fin_tail) = need_room;
-      }
-    }
+    fin_push(sh, done, e.z, lane, err);
     head += static_cast<unsigned>(nb);
     __syncwarp();
     if (lane == 0) *reinterpret_cast<volatile unsigned*>(&sh.bq_head) = head;
@@ -589,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const P prob) {
   } else if (threadIdx.x < kTkBase) {
     bookkeeper_loop(prob, sh);
   } else if (threadIdx.x < kFinBase) {
-    ticketer_loop(prob, sh);
+    ticketer_loop(prob, sh, tab);
   } else if (threadIdx.x < kConsBase) {
     finalizer_loop(prob, sh, tab);
   } else {

@@ -192,6 +192,21 @@ __device__ __forceinline__ int make_info(int b, int kind, int extra) {
   return b | (kind << 16) | (extra << 20);
 }
 
+// Kind of a chain request from its scalar arguments (nd drafts, temperature
+// t, top-k tk): KIND_ARGMAX for t == 0, KIND_TOPK for a filter that keeps
+// fewer than V tokens (0 < tk < V, within the call's bound max_topk),
+// KIND_SOFTMAX otherwise; -1 for invalid arguments (nd outside [0, K], t
+// negative or NaN, tk negative or above max_topk, no draft rows for a
+// sampled request with drafts).
+__device__ __forceinline__ int chain_kind(int nd, float t, int tk, int K, int V, int max_topk,
+                                          bool has_draft) {
+  if (nd < 0 || nd > K || !(t >= 0.f) || tk < 0) return -1;
+  if (t == 0.f) return KIND_ARGMAX;
+  if (!has_draft && nd > 0) return -1;
+  if (tk > 0 && tk < V) return tk <= max_topk ? KIND_TOPK : -1;
+  return KIND_SOFTMAX;
+}
+
 // log2(e)/t as a float pair computed with fp32 divisions only: hi is the
 // quotient rounded down, lo the quotient of the exact (non-negative)
 // remainder.  Both parts are positive, so a -inf logit scales to -inf in

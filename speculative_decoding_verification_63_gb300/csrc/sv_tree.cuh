@@ -20,6 +20,7 @@ struct TreeProblem {
   static constexpr int kAuxBytes = 8;
   static constexpr bool kWarpFinalize = false;
   static constexpr bool kHasDraws = false;
+  static constexpr bool kHasDirectFin = false;
   int n_req, N, M, V, max_depth, es, ipr, chunk_el, max_topk;
   bool bulk;
   const char* target;
