@@ -137,7 +137,7 @@ size_t pos_table_bytes(int n_req, int aux_bytes) {
 template <class P>
 size_t kernel_smem(int n_req) {
   return 128 + static_cast<size_t>(kStages) * kChunkBytes +
-         ((sizeof(Shared) + 15) & ~size_t(15)) + pos_table_bytes(n_req, P::kAuxBytes);
+         ((shared_bytes<P>() + 15) & ~size_t(15)) + pos_table_bytes(n_req, P::kAuxBytes);
 }
 
 template <class P>
@@ -385,9 +385,14 @@ sv_status sv_verify_chain(const sv_chain_args* a, void* workspace, size_t ws_byt
     const sv_status ts = launch_topk(t, static_cast<int>(ctas), st);
     if (ts != SV_OK) return ts;
   }
+  // control CTAs (finalizes and draw finalizes, on SMs that stream nothing):
+  // one per 16 requests, 1 to 8; the rest of the grid streams
+  const int n_ctrl = static_cast<int>(std::min<int64_t>(8, std::max<int64_t>(1, (a->B + 15) / 16)));
   const int64_t items_max = static_cast<int64_t>(a->B) * (2 * a->K + 1) * ipr;
-  const int grid = static_cast<int>(std::min<int64_t>(std::max<int64_t>(items_max, 1), dev.sms));
-  return launch(p, grid, st);
+  const int stream_ctas = static_cast<int>(
+      std::min<int64_t>(std::max<int64_t>(items_max, 1), dev.sms - n_ctrl));
+  p.n_ctrl = n_ctrl;
+  return launch(p, stream_ctas + n_ctrl, st);
 }
 
 sv_status sv_verify_tree(const sv_tree_args* a, void* workspace, size_t ws_bytes,

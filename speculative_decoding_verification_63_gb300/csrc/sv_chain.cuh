@@ -35,7 +35,9 @@ struct ChainProblem {
   static constexpr bool kWarpFinalize = true;
   static constexpr bool kHasDraws = true;
   static constexpr bool kHasDirectFin = true;  // top-k requests: finalize only
+  static constexpr bool kCtrl = true;          // finalizes run on control CTAs
   int n_req, K, V, es, ipr, chunk_el, max_topk;
+  int n_ctrl;        // control CTAs (the last n_ctrl of the grid); they stream nothing
   int ipr2, chunk2;  // draw pass: chunks per row pair, tokens per chunk
   bool bulk;
   const char* target;
@@ -228,7 +230,29 @@ struct ChainProblem {
         }
         tot[s] = seg_sum(xp, xq, t0);
       }
-    } else if (bulk) {
+    } else {
+      return consume_resid_cold(mt, sp, empty_bar, ctid, lane);
+    }
+    return make_float4(tot[0], tot[1], tot[2], tot[3]);
+  }
+
+  // The draw pass for fp32 logits or rows that were not staged: out of line,
+  // so the streaming loop's code stays compact.
+  __device__ __forceinline__ float4 consume_resid_cold(const StageMeta& mt, const unsigned char* sp,
+                                                    uint64_t* empty_bar, int ctid, int lane) const {
+    const int warp = ctid >> 5;
+    const int spw = segs_per_chunk() / kGroupWarps;  // kSpwF32 (fp32) or kSpwBf16
+    const int mode = mt.sub;
+    const ResidParams r{mt.aux.x, mt.aux.y, mt.aux.z, mt.aux.w, Scale2{mt.c_hi, mt.c_lo}, mode};
+    float tot[4] = {0.f, 0.f, 0.f, 0.f};
+    auto seg_sum = [&](const float* xp, const float* xq, int t0) {
+      float w[8];
+      const float ls = resid_weights8(xp, xq, t0, mt.n_el, r, w);
+      return __shfl_sync(0xffffffffu, warp_incl_scan_rn(ls, lane), 31);
+    };
+    const char* pb = reinterpret_cast<const char*>(sp);
+    const char* qb = pb + kChunkBytes / 2;
+    if (bulk) {
       float4 pv[kSpwF32][2], qv[kSpwF32][2];
 #pragma unroll
       for (int s = 0; s < kSpwF32; ++s) {
@@ -301,8 +325,37 @@ struct ChainProblem {
     else if (info_kind(tab.info[code]) == KIND_TOPK) topk_finalize(tab, code, lane, wf);
     else request_finalize(sh, tab, code, lane, wf);
   }
+  // Control CTAs: the finalize of position pos once every chunk of its rows
+  // is booked (returns 1 when it published a draw), and the draw finalize
+  // once every chunk of that draw is booked.  The waits poll the request's
+  // ticket with acquire loads and are bounded.
+  __device__ int ctrl_request(Shared& sh, const PosTables& tab, int pos, int lane,
+                              WarpFin& wf) const {
+    const int info = tab.info[pos];
+    const int b = info_req(info), kind = info_kind(info);
+    const int rows = tab.rstart[pos + 1] - tab.rstart[pos];
+    if (kind == KIND_TOPK) {
+      topk_finalize(tab, pos, lane, wf);
+      return 0;
+    }
+    if (rows == 0) return 0;  // invalid arguments: failed in the preamble
+    if (!wait_ticket(sh, ws.tickets + b, static_cast<unsigned>(rows * ipr), lane)) {
+      if (lane == 0) write_failed(b, 0x10);
+      return 0;
+    }
+    return request_finalize(sh, tab, pos, lane, wf);
+  }
+  __device__ void ctrl_draw(Shared& sh, const PosTables& tab, int pos, int lane,
+                            WarpFin& wf) const {
+    const int b = info_req(tab.info[pos]);
+    if (!wait_ticket(sh, ws.tickets + kDrawTicketBase + b, static_cast<unsigned>(ipr2), lane)) {
+      if (lane == 0) write_failed(b, 0x10);
+      return;
+    }
+    draw_finalize(b, lane, wf);
+  }
   __device__ void topk_finalize(const PosTables& tab, int pos, int lane, WarpFin& wf) const;
-  __device__ void request_finalize(Shared& sh, const PosTables& tab, int pos, int lane,
+  __device__ int request_finalize(Shared& sh, const PosTables& tab, int pos, int lane,
                                    WarpFin& wf) const;
   __device__ void draw_finalize(int b, int lane, WarpFin& wf) const;
   __device__ void last_cta_reset() const {}
@@ -346,7 +399,9 @@ __device__ __forceinline__ void merge_rows(const float2* partials, int r0, int n
       float sum = 0.f;
       if (!nan && M != kNegInf) {
         for (int c0 = 0; c0 < ipr; c0 += 8) {
-          if (c0 > 0) {
+          // t holds the last batch of the maximum pass: reload unless that
+          // batch is the first (a row of at most eight chunks)
+          if (c0 > 0 || ipr > 8) {
 #pragma unroll
             for (int k = 0; k < 8; ++k)
               t[k] = c0 + k < ipr ? __ldcg(pp + c0 + k) : make_float2(kNegInf, 0.f);
@@ -363,7 +418,7 @@ __device__ __forceinline__ void merge_rows(const float2* partials, int r0, int n
   __syncwarp();
 }
 
-__device__ void ChainProblem::request_finalize(Shared& sh, const PosTables& tab, int pos,
+__device__ int ChainProblem::request_finalize(Shared& sh, const PosTables& tab, int pos,
                                                int lane, WarpFin& wf) const {
   const int info = tab.info[pos];
   const int b = info_req(info), kind = info_kind(info), nd = info_extra(info);
@@ -433,6 +488,7 @@ __device__ void ChainProblem::request_finalize(Shared& sh, const PosTables& tab,
     out_tokens[static_cast<size_t>(b) * (K + 1) + i] = v;
   }
   __syncwarp();  // every lane's outputs before lane 0's release below
+  int drew = 0;
   if (lane == 0) {
     out_len[b] = err ? 0 : n + 1;
     accept_len[b] = err ? 0 : n;
@@ -462,9 +518,11 @@ __device__ void ChainProblem::request_finalize(Shared& sh, const PosTables& tab,
       fence_acq_rel_gpu();  // the job and the outputs before the entry
       const unsigned d = atomicAdd(&ws.hdr->draw_reserve, 1u);
       st_relaxed(ws.draws + d, entry);
+      drew = entry > 0 ? 1 : 0;
     }
   }
-  __syncwarp();
+  // 1 when a draw was published (its draw finalize follows its draw pass)
+  return __shfl_sync(0xffffffffu, drew, 0);
 }
 
 // Lane l's 16 segment sums of page g (segments [512 g + 16 l, +16)), zero

@@ -1,23 +1,20 @@
 // sv_kernel.cuh -- the persistent verification kernel, generic over the
 // problem (chain or tree).
 //
-// One CTA per SM, five warp roles (control warps first, so that the warp
+// One CTA per SM, five or six warp roles (control warps first, so that the warp
 // schedulers, which favour lower warp ids, serve them ahead of the
 // always-ready consumers):
 //   warp  0      producer: moves chunks into the 4-stage ring with 1-D bulk
-//                copies: first the CTA's share of the main pass (chunks
-//                blockIdx.x, blockIdx.x + gridDim.x, ...), and draw-pass
-//                chunks claimed from a global counter as soon as their draws
-//                are published (ahead of the next main-pass chunk); claim g
-//                is chunk g % ipr2 of the (g / ipr2)-th entry of the global
-//                draw list, where every sampled request's finalize puts one
-//                entry (its draw, or -1 if it failed); claims beyond the
-//                number of sampled requests lapse.  The 32 lanes work out the main-pass
-//                chunks 32 at a time, each keeping its chunk's metadata in
-//                registers; each lane then puts its own chunk into the ring
-//                (16-byte stores, no loads) and issues the bulk copy.  With
-//                nothing left the producer ends the stream with one sentinel
-//                per consumer group.
+//                copies: the CTA's share of the main pass (chunks
+//                blockIdx.x + j G over the G streaming CTAs), and, ahead of
+//                the next main-pass chunk, every draw-pass chunk the scout
+//                has left in the shared mailbox.  The 32 lanes work out the
+//                main-pass chunks 32 at a time, each keeping its chunk's
+//                metadata in registers; each then puts its own chunk into
+//                the ring (16-byte stores) and issues the bulk copy.
+//                The producer reads only shared memory, so it never waits on
+//                a global load.  With nothing left it ends the stream with
+//                one sentinel per consumer group.
 //   warp  1      bookkeeper: takes result slots in order, combines the 8
 //                per-warp partials of a chunk (max first, one rescale, a
 //                sum) or keeps the residual segment sums, stores them and
@@ -25,9 +22,17 @@
 //   warp  2      ticket warp: takes booked chunks in lane-parallel batches,
 //                fences, bumps the tickets; a completed request or residual
 //                draw joins the finalize list.
-//   warps 3..6   finalizers: take finalize-list entries (each warp on its
-//                own, or the four together for problems that need a group)
-//                while the consumers keep streaming.
+//   warp  6      draw scout (problems with draw passes; otherwise the
+//                fourth finalizer): takes draw-pass claims from a global counter
+//                (claim g is chunk g % ipr2 of the (g / ipr2)-th entry of the
+//                global draw list, where every sampled request's finalize
+//                puts one entry: its draw, or -1 if it failed), waits for the
+//                entry, fetches the job, plans the chunk and leaves it in the
+//                mailbox; claims beyond the number of sampled requests lapse.
+//   warps 3..5   finalizers (3..6 without draw passes): take finalize-list
+//                entries (each warp on its own, or the four together for
+//                problems that need a group) while the consumers keep
+//                streaming.
 //   warps 7..22  consumers, in two groups of eight that take alternate
 //                chunks (so each group has two chunk times per chunk): each
 //                warp reduces its eighth of the chunk, releases the stage as
@@ -111,6 +116,67 @@ __device__ __forceinline__ void flag_timeout(Shared& sh, int* err) {
   record_error(err, 0x10);
 }
 
+// Wait, bounded, until the ticket counter reaches `need`: lane 0 polls it
+// with acquire loads and back-off, then the warp synchronises, so every
+// lane's later loads see what the completing chunks published.  Returns
+// false in every lane when the wait expired.
+__device__ __forceinline__ bool wait_ticket(Shared& sh, const unsigned* ticket, unsigned need,
+                                            int lane) {
+  int ok = 1;
+  if (lane == 0 && ld_acquire(ticket) != need) {
+    const uint64_t t0 = globaltimer_ns();
+    unsigned backoff = 32;
+    ok = 0;
+    for (;;) {
+      __nanosleep(backoff);
+      if (ld_acquire(ticket) == need) {
+        ok = 1;
+        break;
+      }
+      if (globaltimer_ns() - t0 > wait_limit(sh)) {
+        sh.timed_out = 1;
+        break;
+      }
+      backoff = min(backoff * 2u, 256u);
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
+// Control CTAs (problems with kCtrl): the last n_ctrl CTAs of the grid
+// stream nothing; the main pass is spread over the others.
+template <class P>
+__device__ __forceinline__ unsigned n_ctrl_of(const P& prob) {
+  if constexpr (P::kCtrl) return static_cast<unsigned>(prob.n_ctrl);
+  else return 0u;
+}
+
+// Metadata of main-pass chunk `item` (row item / ipr, piece item % ipr);
+// `hint` is the position of a nearby earlier item (or -1).
+template <class P>
+__device__ __forceinline__ void plan_chunk(const P& prob, const PosTables& tab, int n_pos,
+                                           unsigned item, int& hint, PlanRec& rec) {
+  StageMeta& mt = rec.s.m;
+  ResMeta& rm = rec.s.r;
+  const int row = static_cast<int>(item / prob.ipr);
+  const int chunk = static_cast<int>(item % prob.ipr);
+  const int pos = find_pos(tab.rstart, n_pos, row, hint);
+  hint = pos;
+  mt.item = static_cast<int>(item);
+  mt.pos = pos;
+  mt.el_base = chunk * prob.chunk_el;
+  mt.n_el = min(prob.chunk_el, prob.V - mt.el_base);
+  mt.src2 = nullptr;
+  rm.slot = row * prob.ipr + chunk;
+  prob.fill_stage(tab, row - tab.rstart[pos], mt, rm);
+  rm.item = mt.item;
+  rm.kind = mt.kind;
+  rm.c_hi = mt.c_hi;
+  rm.c_lo = mt.c_lo;
+}
+
 template <class P>
 __device__ void producer_loop(const P& prob, Shared& sh, const PosTables& tab,
                               unsigned char* stages) {
@@ -120,7 +186,6 @@ __device__ void producer_loop(const P& prob, Shared& sh, const PosTables& tab,
   const int n_pos = sh.n_pos;
   const int n_rows = tab.rstart[n_pos];
   const unsigned n_items = static_cast<unsigned>(n_rows) * static_cast<unsigned>(prob.ipr);
-  const unsigned G = gridDim.x;
   int it = 0;                 // ring position
 
   // Put a planned chunk into the ring; executed by the one lane holding the
@@ -144,144 +209,100 @@ __device__ void producer_loop(const P& prob, Shared& sh, const PosTables& tab,
       const uint32_t bytes = static_cast<uint32_t>(m.n_el * prob.es);
       unsigned char* dst = stages + static_cast<size_t>(stage) * kChunkBytes;
       mbar_arrive_expect_tx(&sh.full[stage], m.src2 ? 2u * bytes : bytes);
-      bulk_copy_g2s(dst, m.src, bytes, &sh.full[stage]);
-      if (m.src2) bulk_copy_g2s(dst + kChunkBytes / 2, m.src2, bytes, &sh.full[stage]);
+      if (m.src2 == nullptr) {
+        bulk_copy_g2s_hint(dst, m.src, bytes, &sh.full[stage], policy_evict_first());
+      } else {
+        bulk_copy_g2s(dst, m.src, bytes, &sh.full[stage]);
+        bulk_copy_g2s(dst + kChunkBytes / 2, m.src2, bytes, &sh.full[stage]);
+      }
     } else {
       mbar_arrive(&sh.full[stage]);
     }
   };
 
-  // Draw-pass claims run alongside the main pass (lane 0): a claim is taken
-  // when the CTA starts; once per issued main-pass chunk the claim machine
-  // advances one step (read the claim, poll the draw list, fetch the job,
-  // plan the chunk); a planned draw chunk goes into the ring ahead of the
-  // next main-pass chunk and the next claim is taken.  Claim g is chunk
-  // g % ipr2 of the (g / ipr2)-th entry of the draw list.  Every sampled
-  // request puts exactly one entry there (-1 if it failed), so claims beyond
-  // the number of sampled requests lapse at once and every other claim's
-  // entry is bound to appear.
-  enum { D_NONE, D_CLAIMED, D_POLL, D_JOB };
-  int dstate = D_NONE;
-  unsigned dclaim = 0;
-  int poll = 0;
-  P2Job job{};
-  PlanRec drec;
-  const unsigned cap = P::kHasDraws ? static_cast<unsigned>(sh.n_draw_cap) : 0u;
-  if (lane == 0 && cap > 0) {
-    dclaim = atomicAdd(&hdr->work_counter, 1u);
-    dstate = D_CLAIMED;
-  }
-  auto draw_step = [&]() -> bool {
+  // Draw-pass chunks planned by the scout wait in the shared mailbox.  The
+  // lane that issues the next ring position first moves every waiting record
+  // into the ring, then its own chunk.  The ring position and the mailbox
+  // head live in shared memory, so consecutive positions are handed from
+  // lane to lane with one __syncwarp and no other warp-wide operation (a
+  // collective per chunk measurably slowed the producer).  Only shared
+  // memory is read here: the producer never waits on global memory.
+  auto issue_mailbox = [&](int at) -> int {  // one lane; returns the next position
     if constexpr (P::kHasDraws) {
-      const unsigned d = dclaim / static_cast<unsigned>(prob.ipr2);
-      if (dstate == D_CLAIMED) {
-        if (d >= cap) {
-          dstate = D_NONE;
-          return false;
+      const unsigned t = vload(sh.mb_tail);
+      unsigned h = vload(sh.mb_head);
+      if (t != h) {
+        __threadfence_block();  // the records before their use
+        for (; h != t; ++h) {
+          PlanRec r;
+          const uint4* src = reinterpret_cast<const uint4*>(&sh.mb[h % kMbCap]);
+#pragma unroll
+          for (int q = 0; q < kStageWords + kResWords16; ++q) r.v[q] = src[q];
+          __threadfence_block();
+          *reinterpret_cast<volatile unsigned*>(&sh.mb_head) = h + 1u;
+          issue_own(r, at++);
         }
-        poll = ld_relaxed(prob.ws.draws + d);
-        dstate = D_POLL;
-      } else if (dstate == D_POLL) {
-        if (poll > 0) {
-          // the entry is there: read it again with acquire (the job was
-          // published before it), then fetch the job
-          const int e = ld_acquire(prob.ws.draws + d);
-          job = prob.load_job(e - 1);
-          dstate = D_JOB;
-        } else if (poll < 0) {
-          // a request that failed: its draw has no chunks, take a new claim
-          dclaim = atomicAdd(&hdr->work_counter, 1u);
-          dstate = D_CLAIMED;
-        } else {
-          poll = ld_relaxed(prob.ws.draws + d);
-        }
-      } else if (dstate == D_JOB) {
-        StageMeta& mt = drec.s.m;
-        ResMeta& rm = drec.s.r;
-        mt.item = 0x7fffffff;
-        mt.pos = -1;
-        mt.src2 = nullptr;
-        prob.fill_resid(job, static_cast<int>(dclaim % static_cast<unsigned>(prob.ipr2)), mt, rm);
-        rm.item = mt.item;
-        rm.kind = mt.kind;
-        rm.c_hi = mt.c_hi;
-        rm.c_lo = mt.c_lo;
-        dclaim = atomicAdd(&hdr->work_counter, 1u);
-        dstate = D_CLAIMED;
-        return true;
       }
     }
-    return false;
+    return at;
   };
 
-  // Main pass: this CTA's share (chunks blockIdx.x + j G), worked out 32 at
-  // a time, one chunk per lane and held in that lane's registers, then
-  // issued in order, each by its own lane.
+  // Main pass: this CTA's share (chunks blockIdx.x + j G over the G
+  // streaming CTAs), worked out 32 at a time, one chunk per lane and held
+  // in that lane's registers, then issued in order, each by its own lane.
+  const unsigned G = gridDim.x - n_ctrl_of(prob);
   for (unsigned base = blockIdx.x; base < n_items; base += 32u * G) {
     const int cnt = static_cast<int>(min(32u, (n_items - base + G - 1u) / G));
     PlanRec rec;
-    if (lane < cnt) {
-      const unsigned item = base + static_cast<unsigned>(lane) * G;
-      StageMeta& mt = rec.s.m;
-      ResMeta& rm = rec.s.r;
-      const int row = static_cast<int>(item / prob.ipr);
-      const int chunk = static_cast<int>(item % prob.ipr);
-      const int pos = find_pos(tab.rstart, n_pos, row, -1);
-      mt.item = static_cast<int>(item);
-      mt.pos = pos;
-      mt.el_base = chunk * prob.chunk_el;
-      mt.n_el = min(prob.chunk_el, prob.V - mt.el_base);
-      mt.src2 = nullptr;
-      rm.slot = row * prob.ipr + chunk;
-      prob.fill_stage(tab, row - tab.rstart[pos], mt, rm);
-      rm.item = mt.item;
-      rm.kind = mt.kind;
-      rm.c_hi = mt.c_hi;
-      rm.c_lo = mt.c_lo;
-    }
+    int hint = -1;
+    if (lane < cnt) plan_chunk(prob, tab, n_pos, base + static_cast<unsigned>(lane) * G, hint, rec);
     for (int k = 0; k < cnt; ++k) {
-      int have_draw = 0;
-      if (lane == 0 && dstate != D_NONE) have_draw = draw_step() ? 1 : 0;
-      have_draw = __shfl_sync(0xffffffffu, have_draw, 0);
-      if (have_draw) {
-        if (lane == 0) issue_own(drec, it);
-        ++it;
+      if (lane == k) {
+        int at = static_cast<int>(vload(sh.p_it));
+        at = issue_mailbox(at);
+        issue_own(rec, at);
+        *reinterpret_cast<volatile unsigned*>(&sh.p_it) = static_cast<unsigned>(at + 1);
       }
-      if (lane == k) issue_own(rec, it);
-      ++it;
+      // ring positions are issued strictly in order: no lane goes on to
+      // the next position before this one is in the ring
+      __syncwarp();
     }
-    __syncwarp();
   }
 
   if constexpr (P::kHasDraws) {
-    // The rest of the draw pass: lane 0 runs the claim machine until a chunk
-    // is planned or the claim lapses (beyond the sampled requests).
+    // The rest of the draw pass (lane 0): move the scout's records until it
+    // is done.
     if (lane == 0) {
+      int at = static_cast<int>(vload(sh.p_it));
       uint64_t t0 = 0;
-      unsigned backoff = 64;
-      while (dstate != D_NONE) {
-        if (draw_step()) {
-          issue_own(drec, it);
-          ++it;
+      unsigned backoff = 32;
+      for (;;) {
+        const int before = at;
+        at = issue_mailbox(at);
+        if (at != before) {
           t0 = 0;
-          backoff = 64;
+          backoff = 32;
           continue;
         }
-        if (dstate == D_POLL && poll == 0) {
-          const uint64_t now = globaltimer_ns();
-          if (t0 == 0) t0 = now;
-          if (now - t0 > wait_limit(sh)) {
-            flag_timeout(sh, err);
-            dstate = D_NONE;
-            break;
-          }
-          __nanosleep(backoff);
-          backoff = min(backoff * 2u, 512u);
+        if (vload(sh.sc_done) != 0u) {
+          __threadfence_block();
+          if (vload(sh.mb_tail) == vload(sh.mb_head)) break;
+          continue;
         }
+        const uint64_t now = globaltimer_ns();
+        if (t0 == 0) t0 = now;
+        if (now - t0 > 2 * wait_limit(sh)) {
+          flag_timeout(sh, err);
+          break;
+        }
+        __nanosleep(backoff);
+        backoff = min(backoff * 2u, 256u);
       }
+      *reinterpret_cast<volatile unsigned*>(&sh.p_it) = static_cast<unsigned>(at);
     }
-    it = __shfl_sync(0xffffffffu, it, 0);
+    __syncwarp();
   }
+  it = static_cast<int>(vload(sh.p_it));
 
   // end of stream: one sentinel per consumer group (the bookkeeper stops at
   // the first)
@@ -298,6 +319,99 @@ __device__ void producer_loop(const P& prob, Shared& sh, const PosTables& tab,
     }
   }
   __syncwarp();
+}
+
+// The draw scout (lane 0 of its warp): takes draw-pass claims from the
+// global counter, waits for the claimed draw to be published, fetches its
+// job, plans the chunk and leaves the record in the shared mailbox for the
+// producer.  Claim g is chunk g % ipr2 of the (g / ipr2)-th entry of the
+// draw list, where every sampled request's finalize puts one entry (its
+// draw, or -1 if it failed); claims beyond the number of sampled requests
+// lapse and end the scout.  All its waits on global memory happen here, off
+// the producer's path.
+template <class P>
+__device__ void scout_loop(const P& prob, Shared& sh) {
+  if constexpr (P::kHasDraws) {
+    const int lane = threadIdx.x & 31;
+    WsHeader* hdr = prob.ws.hdr;
+    int* err = &hdr->error;
+    const unsigned cap = static_cast<unsigned>(sh.n_draw_cap);
+    if (lane == 0 && cap > 0) {
+      unsigned tail = 0;
+      unsigned cached_d = 0xffffffffu;
+      bool cached_failed = false;
+      P2Job job{};
+      for (;;) {
+        // room in the mailbox
+        if (tail - vload(sh.mb_head) >= static_cast<unsigned>(kMbCap)) {
+          const uint64_t t0 = globaltimer_ns();
+          bool ok = true;
+          while (tail - vload(sh.mb_head) >= static_cast<unsigned>(kMbCap)) {
+            if (globaltimer_ns() - t0 > wait_limit(sh)) {
+              ok = false;
+              break;
+            }
+            __nanosleep(64);
+          }
+          if (!ok) {
+            flag_timeout(sh, err);
+            break;
+          }
+        }
+        const unsigned g = atomicAdd(&hdr->work_counter, 1u);
+        const unsigned d = g / static_cast<unsigned>(prob.ipr2);
+        if (d >= cap) break;
+        if (d != cached_d) {
+          int e = ld_relaxed(prob.ws.draws + d);
+          if (e == 0) {
+            const uint64_t t0 = globaltimer_ns();
+            unsigned backoff = 32;
+            while (e == 0) {
+              if (globaltimer_ns() - t0 > wait_limit(sh)) break;
+              __nanosleep(backoff);
+              backoff = min(backoff * 2u, 256u);
+              e = ld_relaxed(prob.ws.draws + d);
+            }
+            if (e == 0) {
+              flag_timeout(sh, err);
+              break;
+            }
+          }
+          cached_d = d;
+          cached_failed = e < 0;
+          if (!cached_failed) {
+            // read the entry again with acquire (the job was published
+            // before it), then fetch the job
+            e = ld_acquire(prob.ws.draws + d);
+            job = prob.load_job(e - 1);
+          }
+        }
+        if (cached_failed) continue;  // a failed request's draw has no chunks
+        PlanRec rec;
+        StageMeta& mt = rec.s.m;
+        ResMeta& rm = rec.s.r;
+        mt.item = 0x7fffffff;
+        mt.pos = -1;
+        mt.src2 = nullptr;
+        prob.fill_resid(job, static_cast<int>(g % static_cast<unsigned>(prob.ipr2)), mt, rm);
+        rm.item = mt.item;
+        rm.kind = mt.kind;
+        rm.c_hi = mt.c_hi;
+        rm.c_lo = mt.c_lo;
+        uint4* dst = reinterpret_cast<uint4*>(&sh.mb[tail % kMbCap]);
+#pragma unroll
+        for (int q = 0; q < kStageWords + kResWords16; ++q) dst[q] = rec.v[q];
+        __threadfence_block();
+        ++tail;
+        *reinterpret_cast<volatile unsigned*>(&sh.mb_tail) = tail;
+      }
+    }
+    if (lane == 0) {
+      __threadfence_block();
+      *reinterpret_cast<volatile unsigned*>(&sh.sc_done) = 1u;
+    }
+    __syncwarp();
+  }
 }
 
 template <class P>
@@ -418,7 +532,7 @@ template <class P>
 __device__ void ticketer_loop(const P& prob, Shared& sh, const PosTables& tab) {
   int* err = &prob.ws.hdr->error;
   const int lane = threadIdx.x & 31;
-  if constexpr (P::kHasDirectFin) {
+  if constexpr (P::kHasDirectFin && !P::kCtrl) {
     const int G = static_cast<int>(gridDim.x);
     for (int p0 = static_cast<int>(blockIdx.x); p0 < sh.n_pos; p0 += 32 * G) {
       const int p = p0 + lane * G;
@@ -458,7 +572,7 @@ __device__ void ticketer_loop(const P& prob, Shared& sh, const PosTables& tab) {
       const unsigned old = atomic_add_acq_rel(&prob.ws.tickets[e.x], 1u);
       done = old + 1u == static_cast<unsigned>(e.y);
     }
-    fin_push(sh, done, e.z, lane, err);
+    if constexpr (!P::kCtrl) fin_push(sh, done, e.z, lane, err);
     head += static_cast<unsigned>(nb);
     __syncwarp();
     if (lane == 0) *reinterpret_cast<volatile unsigned*>(&sh.bq_head) = head;
@@ -557,8 +671,38 @@ __device__ void finalizer_loop(const P& prob, Shared& sh, const PosTables& tab) 
   }
 }
 
+// A control CTA: every warp takes the positions c + n_ctrl (warp + nw k)
+// (c = this control CTA's index), waits for each one's rows and finalizes
+// it, then waits for the draw passes of the ones that published a draw and
+// runs their draw finalizes.  Control CTAs share no SM with the streaming
+// roles, so a finalize runs as soon as its last chunk is booked.  The
+// per-warp scratch lives in the unused chunk ring.
+template <class P>
+__device__ void control_loop(const P& prob, Shared& sh, const PosTables& tab,
+                             unsigned char* scratch) {
+  if constexpr (P::kCtrl) {
+    constexpr int nw = kThreads / 32;
+    const int warp = static_cast<int>(threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    const int n_ctrl = prob.n_ctrl;
+    const int c = static_cast<int>(blockIdx.x) - (static_cast<int>(gridDim.x) - n_ctrl);
+    WarpFin& wf = reinterpret_cast<WarpFin*>(scratch)[warp];
+    const int first = c + n_ctrl * warp, step = n_ctrl * nw;
+    unsigned long long drew = 0ull;  // positions of this warp that published a draw
+    int k = 0;
+    for (int p = first; p < sh.n_pos; p += step, ++k)
+      if (prob.ctrl_request(sh, tab, p, lane, wf) && k < 64) drew |= 1ull << k;
+    k = 0;
+    for (int p = first; p < sh.n_pos && k < 64; p += step, ++k)
+      if ((drew >> k) & 1ull) prob.ctrl_draw(sh, tab, p, lane, wf);
+  }
+}
+
 template <class P>
 __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const P prob) {
+  static_assert(kThreads / 32 * sizeof(WarpFin) <= static_cast<size_t>(kStages) * kChunkBytes,
+                "control CTAs keep one warp scratch per warp in the chunk ring");
+  static_assert(!P::kHasDraws || P::kWarpFinalize,
+                "the draw scout takes a finalizer warp: group finalizes need all four");
   extern __shared__ __align__(1024) unsigned char smem_dyn[];
   // Launched with programmatic stream serialisation: wait for the previous
   // work on the stream (which may have produced the inputs, and used the
@@ -570,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const P prob) {
   unsigned char* smem_raw = smem_dyn + ((128u - (smem_u32(smem_dyn) & 127u)) & 127u);
   unsigned char* stages = smem_raw;
   Shared& sh = *reinterpret_cast<Shared*>(smem_raw + kStages * kChunkBytes);
-  unsigned char* tail = smem_raw + kStages * kChunkBytes + ((sizeof(Shared) + 15) & ~size_t(15));
+  unsigned char* tail = smem_raw + kStages * kChunkBytes + ((shared_bytes<P>() + 15) & ~size_t(15));
   // tables in decreasing alignment: aux (16- or 8-byte entries) at the
   // 16-byte aligned tail, then the float2 scales, then the int tables
   PosTables tab;
@@ -595,20 +739,25 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const P prob) {
     sh.bk_done = 0u;
     sh.bq_tail = sh.bq_head = 0u;
     sh.tk_done = 0u;
+    sh.p_it = 0u;
+    if (P::kHasDraws) sh.mb_tail = sh.mb_head = sh.sc_done = 0u;
     sh.fin_cmd = -1;
     sh.n_draw_cap = 0;
   }
   prob.preamble(sh, tab, scan_tmp);
   __syncthreads();
 
-  if (threadIdx.x < kBkBase) {
+  if (P::kCtrl && blockIdx.x >= gridDim.x - n_ctrl_of(prob)) {
+    control_loop(prob, sh, tab, stages);
+  } else if (threadIdx.x < kBkBase) {
     producer_loop(prob, sh, tab, stages);
   } else if (threadIdx.x < kTkBase) {
     bookkeeper_loop(prob, sh);
   } else if (threadIdx.x < kFinBase) {
     ticketer_loop(prob, sh, tab);
   } else if (threadIdx.x < kConsBase) {
-    finalizer_loop(prob, sh, tab);
+    if (P::kHasDraws && threadIdx.x >= kScBase) scout_loop(prob, sh);
+    else if (!P::kCtrl) finalizer_loop(prob, sh, tab);
   } else {
     consumer_loop(prob, sh, stages);
   }

@@ -15,6 +15,8 @@
 // inside a CTA is an mbarrier; no CTA ever waits for another.
 #pragma once
 
+#include <stddef.h>
+
 #include "sv_device.cuh"
 
 namespace sv {
@@ -36,7 +38,9 @@ constexpr int kFinThreads = kFinWarps * 32;
 constexpr int kProducerBase = 0;              // the producer warp
 constexpr int kBkBase = 32;                   // bookkeeper warp
 constexpr int kTkBase = 64;                   // ticket warp
-constexpr int kFinBase = 96;                  // finalizer group
+constexpr int kFinBase = 96;                  // finalizer group (problems with draws: the
+                                              // last of its warps is the draw scout)
+constexpr int kScBase = kFinBase + 3 * 32;    // draw scout warp (problems with draws)
 constexpr int kConsBase = kFinBase + kFinThreads;  // consumer warps
 constexpr int kThreads = kConsBase + kConsumers;
 constexpr int kRSeg = 256;                   // draw pass: tokens per segment (8 per lane)
@@ -44,6 +48,7 @@ constexpr int kPageSeg = 512;                // draw finalize: segments per page
 constexpr int kMaxPages = 8;                 // => at most 4096 segments (V <= 2^20)
 constexpr int kFinCap = 128;                  // requests awaiting their finalize
 constexpr int kBqCap = 256;                   // booked chunks awaiting their ticket
+constexpr int kMbCap = 4;                     // planned draw chunks awaiting the producer
 constexpr int kSegEl = 1024;        // inverse-CDF segment: 32 lanes x 32 elements
 constexpr int kMaxSeg = 1024;       // => V <= 2^20
 constexpr int kMaxRowsPerReq = 128;  // chain: 2K+1 <= 65; tree: N + M <= 128
@@ -64,7 +69,7 @@ constexpr int kFinResid = 0x40000000;  // finalize-list flag: a residual draw (r
 constexpr int kDrawTicketBase = 1024;  // draw tickets follow the request tickets (SV_MAX_B)
 
 struct WsHeader {
-  unsigned int work_counter;  // chunks claimed: main pass, then draw pass
+  unsigned int work_counter;  // draw-pass chunks claimed
   unsigned int done_ctas;
   int error;
   unsigned int draw_reserve;  // entries of the draw list reserved so far
@@ -159,6 +164,7 @@ struct __align__(16) Shared {
   StageMeta meta[kStages];
   ResMeta res_meta[kResSlots];
   float4 res_part[kResSlots][kGroupWarps];
+  unsigned p_it;               // next ring position (producer lanes, in turn)
   int4 bq[kBqCap];             // booked chunks: ticket, count that completes it, finalize code
   unsigned bq_tail;            // entries published (bookkeeper only)
   unsigned bq_head;            // entries ticketed (ticket warp only)
@@ -175,7 +181,18 @@ struct __align__(16) Shared {
   int is_last;    // this CTA finished last
   FinScratch fin;
   WarpFin wfin[kFinWarps];
+  PlanRec mb[kMbCap];          // scout -> producer: planned draw chunks
+  unsigned mb_tail;            // records published (scout only)
+  unsigned mb_head;            // records taken (producer only)
+  unsigned sc_done;            // the scout has no more claims
 };
+
+// Bytes of Shared that a problem uses: the draw mailbox, at the end, only
+// for problems with draw passes.
+template <class P>
+__host__ __device__ constexpr size_t shared_bytes() {
+  return P::kHasDraws ? sizeof(Shared) : offsetof(Shared, mb);
+}
 
 // Per-position tables that follow Shared in dynamic shared memory.
 struct PosTables {
@@ -352,6 +369,7 @@ __device__ __forceinline__ void reduce_chunk_bf16(const StageMeta& mt, const uin
 }
 
 // Generic path: any dtype, chunk either staged (bulk) or read from global.
+// Out of line, so the streaming loop's code stays compact.
 template <int KIND>
 __device__ __forceinline__ void reduce_chunk_generic(const StageMeta& mt, const char* stage,
                                                      bool staged, int es,

@@ -21,6 +21,7 @@ struct TreeProblem {
   static constexpr bool kWarpFinalize = false;
   static constexpr bool kHasDraws = false;
   static constexpr bool kHasDirectFin = false;
+  static constexpr bool kCtrl = false;
   int n_req, N, M, V, max_depth, es, ipr, chunk_el, max_topk;
   bool bulk;
   const char* target;

@@ -72,6 +72,15 @@ def test_chunk_boundaries(V):
     check_chain(wl.make_chain(3, B=8, V=V, seed=V + 1))
 
 
+def test_rows_of_more_than_eight_chunks():
+    """Rows longer than eight 32 KB chunks (bf16 V = 150000: ten chunks;
+    fp32 V = 70000: nine), so a row's partials are merged in several batches."""
+    inp = wl.make_chain(3, B=6, V=150_000, seed=150)
+    inp["temperature"][:] = 1.0  # every request sampled: the (max, sum) merge
+    check_chain(inp)
+    check_chain(wl.make_chain(1, B=4, V=70_000, seed=70))
+
+
 def test_fp32_aligned_rows():
     inp = wl.make_chain(1, B=16, V=12_000, seed=4)
     check_chain(inp)
