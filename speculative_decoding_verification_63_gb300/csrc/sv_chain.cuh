@@ -294,6 +294,26 @@ struct ChainProblem {
     return make_float4(tot[0], tot[1], tot[2], tot[3]);
   }
 
+  // A row chunk's partial as one 64-bit word that control CTAs poll: (max,
+  // sum) for softmax rows, (max, lowest index + 1) for argmax rows.  Never
+  // all zero (a sum is at least 1 unless the maximum is -inf or NaN; the
+  // index word is at least 1), so zero marks a slot not yet written.
+  __device__ void store_partial(int slot, int kind, float2 v) const {
+    const unsigned hi = kind == KIND_ARGMAX ? static_cast<unsigned>(__float_as_int(v.y)) + 1u
+                                            : __float_as_uint(v.y);
+    st_relaxed_u64(reinterpret_cast<unsigned long long*>(ws.partials + slot),
+                   (static_cast<unsigned long long>(hi) << 32) | __float_as_uint(v.x));
+  }
+  // A draw chunk's segment sums of consumer warp w (spw of them), stored
+  // where the draw finalize polls them (sums are >= 0; the finalize fills
+  // the slots with -1 before it publishes the draw).
+  __device__ void store_segsums_warp(int base, int w, float4 v) const {
+    const int spw = segs_per_chunk() / kGroupWarps;
+    float* d = ws.segsums + base + w * spw;
+    const float x[4] = {v.x, v.y, v.z, v.w};
+    for (int k = 0; k < spw; ++k)
+      asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(d + k), "f"(x[k]) : "memory");
+  }
   __device__ void store_segsums(const ResMeta& rm, int lane, float4 v) const {
     const int spw = segs_per_chunk() / kGroupWarps;
     if (lane < kGroupWarps) {
@@ -339,19 +359,81 @@ struct ChainProblem {
       return 0;
     }
     if (rows == 0) return 0;  // invalid arguments: failed in the preamble
-    if (!wait_ticket(sh, ws.tickets + b, static_cast<unsigned>(rows * ipr), lane)) {
+    // the request's chunk partials: rows rstart[pos] .. (lane j polls row j,
+    // the row it merges); zero marks a slot not yet written
+    unsigned long long* w =
+        reinterpret_cast<unsigned long long*>(ws.partials) + static_cast<size_t>(tab.rstart[pos]) * ipr;
+    // the progress count first (one word: cheap to poll), then the words
+    // themselves (the count is not ordered with them)
+    if (!wait_ticket(sh, ws.tickets + b, static_cast<unsigned>(rows * ipr), lane) ||
+        !wait_rows(sh, w, rows, ipr, lane)) {
       if (lane == 0) write_failed(b, 0x10);
       return 0;
     }
-    return request_finalize(sh, tab, pos, lane, wf);
+    const int drew = request_finalize(sh, tab, pos, lane, wf);
+    // leave the slots zero for the next call
+    for (int j = lane; j < rows; j += 32)
+      for (int c = 0; c < ipr; ++c) st_relaxed_u64(w + static_cast<size_t>(j) * ipr + c, 0ull);
+    return drew;
+  }
+  // Wait, bounded, until every word of rows 0..rows-1 (ipr words each) is
+  // nonzero: lane j polls row j (and j + 32, ...).
+  __device__ bool wait_rows(Shared& sh, const unsigned long long* w, int rows, int n,
+                            int lane) const {
+    const uint64_t t0 = globaltimer_ns();
+    unsigned backoff = 32;
+    int next = 0;  // first word of this lane's rows not yet seen written
+    const int mine = rows > lane ? ((rows - 1 - lane) / 32 + 1) * n : 0;
+    for (;;) {
+      while (next < mine) {
+        const int j = lane + 32 * (next / n), c = next % n;
+        if (ld_relaxed_u64(w + static_cast<size_t>(j) * n + c) == 0ull) break;
+        ++next;
+      }
+      if (__all_sync(0xffffffffu, next >= mine)) {
+        __syncwarp();
+        return true;
+      }
+      if (globaltimer_ns() - t0 > (sh.timed_out ? kWaitLimitAfterTimeoutNs : kWaitLimitNs)) {
+        sh.timed_out = 1;
+        return false;
+      }
+      __nanosleep(backoff);
+      backoff = min(backoff * 2u, 256u);
+    }
   }
   __device__ void ctrl_draw(Shared& sh, const PosTables& tab, int pos, int lane,
                             WarpFin& wf) const {
     const int b = info_req(tab.info[pos]);
-    if (!wait_ticket(sh, ws.tickets + kDrawTicketBase + b, static_cast<unsigned>(ipr2), lane)) {
+    // the draw's segment sums, polled in the layout the draw finalize reads
+    // them (lane l: 16 consecutive sums of each page of 512)
+    const int nseg = ipr2 * segs_per_chunk();
+    const float* ss = ws.segsums + static_cast<size_t>(b) * nseg;
+    if (!wait_ticket(sh, ws.tickets + kDrawTicketBase + b,
+                     static_cast<unsigned>(ipr2), lane)) {
       if (lane == 0) write_failed(b, 0x10);
       return;
     }
+    const uint64_t t0 = globaltimer_ns();
+    unsigned backoff = 32;
+    int next = 0;
+    const int npages = (nseg + kPageSeg - 1) / kPageSeg;
+    for (;;) {
+      while (next < npages * 16) {
+        const int i = (next / 16) * kPageSeg + lane * 16 + next % 16;
+        if (i < nseg && !(ld_relaxed_f32(ss + i) >= 0.f)) break;
+        ++next;
+      }
+      if (__all_sync(0xffffffffu, next >= npages * 16)) break;
+      if (globaltimer_ns() - t0 > (sh.timed_out ? kWaitLimitAfterTimeoutNs : kWaitLimitNs)) {
+        sh.timed_out = 1;
+        if (lane == 0) write_failed(b, 0x10);
+        return;
+      }
+      __nanosleep(backoff);
+      backoff = min(backoff * 2u, 256u);
+    }
+    __syncwarp();
     draw_finalize(b, lane, wf);
   }
   __device__ void topk_finalize(const PosTables& tab, int pos, int lane, WarpFin& wf) const;
@@ -380,7 +462,8 @@ __device__ __forceinline__ void merge_rows(const float2* partials, int r0, int n
           t[k] = c0 + k < ipr ? __ldcg(pp + c0 + k)
                               : make_float2(kNegInf, __int_as_float(0x7fffffff));
 #pragma unroll
-        for (int k = 0; k < 8; ++k) v = vi_better(v, VI{t[k].x, __float_as_int(t[k].y)});
+        for (int k = 0; k < 8; ++k)
+          if (c0 + k < ipr) v = vi_better(v, VI{t[k].x, __float_as_int(t[k].y) - 1});
       }
       wf.rm[j] = v.v;
       wf.ridx[j] = v.i;
@@ -486,6 +569,20 @@ __device__ int ChainProblem::request_finalize(Shared& sh, const PosTables& tab, 
       else if (i == n && greedy) v = wf.ridx[n];
     }
     out_tokens[static_cast<size_t>(b) * (K + 1) + i] = v;
+  }
+  if (!greedy && !err) {
+    // the draw's segment sums start at -1: the draw finalize waits for
+    // every one of them to be written (sums are >= 0).  Each lane marks
+    // exactly the sums it polls later (16 consecutive ones of each page of
+    // 512), with GPU-scope stores, so its polls cannot see an older value.
+    const int nseg = ipr2 * segs_per_chunk();
+    float* ss = ws.segsums + static_cast<size_t>(b) * nseg;
+    for (int g = 0; g * kPageSeg < nseg; ++g)
+      for (int k = 0; k < 16; ++k) {
+        const int i = g * kPageSeg + lane * 16 + k;
+        if (i < nseg)
+          asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(ss + i), "f"(-1.f) : "memory");
+      }
   }
   __syncwarp();  // every lane's outputs before lane 0's release below
   int drew = 0;
@@ -692,6 +789,10 @@ __device__ void ChainProblem::draw_finalize(int b, int lane, WarpFin& wf) const 
     ws.tickets[kDrawTicketBase + b] = 0u;
   }
   __syncwarp();
+  // leave the segment sums zero: any part of the workspace may serve another
+  // call's chunk partials, which must start at zero
+  for (int k = lane; k < nseg; k += 32) ss[k] = 0.f;
+  __syncwarp();
 }
 
 // Finalize of a top-k request from the top-k pass's lists: row (b, i) holds
@@ -878,6 +979,13 @@ __device__ void ChainProblem::topk_finalize(const PosTables& tab, int pos, int l
     accept_len[b] = err ? 0 : n;
     if (err) record_error(&ws.hdr->error, err);
   }
+  __syncwarp();
+  // leave the lists and (m, Z) of the request's rows zero (see draw_finalize)
+  for (int j = 0; j < nrows; ++j) {
+    float2* l = const_cast<float2*>(list_of(j));
+    for (int i = lane; i < max_topk; i += 32) l[i] = make_float2(0.f, 0.f);
+  }
+  for (int j = lane; j < nrows; j += 32) const_cast<float2*>(topk_mz)[r0 + j] = make_float2(0.f, 0.f);
   __syncwarp();
 }
 

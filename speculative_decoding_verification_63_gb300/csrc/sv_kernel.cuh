@@ -172,6 +172,7 @@ __device__ __forceinline__ void plan_chunk(const P& prob, const PosTables& tab, 
   rm.slot = row * prob.ipr + chunk;
   prob.fill_stage(tab, row - tab.rstart[pos], mt, rm);
   rm.item = mt.item;
+  mt.slot = rm.slot;
   rm.kind = mt.kind;
   rm.c_hi = mt.c_hi;
   rm.c_lo = mt.c_lo;
@@ -395,7 +396,8 @@ __device__ void scout_loop(const P& prob, Shared& sh) {
         mt.src2 = nullptr;
         prob.fill_resid(job, static_cast<int>(g % static_cast<unsigned>(prob.ipr2)), mt, rm);
         rm.item = mt.item;
-        rm.kind = mt.kind;
+        mt.slot = rm.slot;
+              rm.kind = mt.kind;
         rm.c_hi = mt.c_hi;
         rm.c_lo = mt.c_lo;
         uint4* dst = reinterpret_cast<uint4*>(&sh.mb[tail % kMbCap]);
@@ -454,6 +456,28 @@ __device__ void bookkeeper_loop(const P& prob, Shared& sh) {
                                         : make_float4(kNegInf, 0.f, 0.f, 0.f);
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.res_free[rs]);
+    if constexpr (P::kCtrl) {
+      // Control CTAs poll: the results go straight to the workspace (words
+      // the pollers check themselves), then a relaxed count that tells them
+      // when to look.  No fence, no queue, nothing waits here.
+      if (rm.kind == KIND_RESID_PASS) {
+        if (lane < kGroupWarps) prob.store_segsums_warp(rm.slot, lane, p);
+      } else {
+        float2 tot;
+        if (rm.kind == KIND_ARGMAX) {
+          const VI v = warp_reduce_vi(VI{p.x, lane < kGroupWarps ? __float_as_int(p.y)
+                                                                 : 0x7fffffff});
+          tot = make_float2(v.v, __int_as_float(v.i));
+        } else {
+          const MS v = warp_reduce_ms(MS{p.x, p.y}, Scale2{rm.c_hi, rm.c_lo});
+          tot = make_float2(v.m, v.s);
+        }
+        if (lane == 0) prob.store_partial(rm.slot, rm.kind, tot);
+      }
+      __syncwarp();
+      if (lane == 0) red_relaxed_add(prob.ws.tickets + rm.tkt, 1u);
+      continue;
+    }
     if (rm.kind == KIND_RESID_PASS) {
       // draw-pass chunk: the segment sums of the consumer warps, in order
       if constexpr (P::kHasDraws) prob.store_segsums(rm, lane, p);
@@ -566,13 +590,24 @@ __device__ void ticketer_loop(const P& prob, Shared& sh, const PosTables& tab) {
     __threadfence_block();  // the entries (and the bookkeeper's stores) before reading them
     const int nb = static_cast<int>(min(tail - head, 32u));
     const int4 e = lane < nb ? sh.bq[(head + lane) % kBqCap] : make_int4(0, 0, 0, 0);
-    fence_acq_rel_gpu();  // the partials (stored by the bookkeeper) -> GPU scope before the tickets
-    bool done = false;
-    if (lane < nb) {
-      const unsigned old = atomic_add_acq_rel(&prob.ws.tickets[e.x], 1u);
-      done = old + 1u == static_cast<unsigned>(e.y);
+    if constexpr (P::kCtrl) {
+      // Control CTAs poll the tickets, so nothing here needs the counts: one
+      // release reduction per distinct ticket of the batch (lanes with the
+      // same ticket merged), no fence and no round trip.  The release makes
+      // the partials the bookkeeper stored (seen through the queue) visible
+      // before the count that covers them.
+      const unsigned same = __match_any_sync(0xffffffffu, lane < nb ? e.x : -1);
+      if (lane < nb && lane == __ffs(same) - 1)
+        red_release_add(&prob.ws.tickets[e.x], static_cast<unsigned>(__popc(same)));
+    } else {
+      fence_acq_rel_gpu();  // the partials (stored by the bookkeeper) -> GPU scope before the tickets
+      bool done = false;
+      if (lane < nb) {
+        const unsigned old = atomic_add_acq_rel(&prob.ws.tickets[e.x], 1u);
+        done = old + 1u == static_cast<unsigned>(e.y);
+      }
+      fin_push(sh, done, e.z, lane, err);
     }
-    if constexpr (!P::kCtrl) fin_push(sh, done, e.z, lane, err);
     head += static_cast<unsigned>(nb);
     __syncwarp();
     if (lane == 0) *reinterpret_cast<volatile unsigned*>(&sh.bq_head) = head;
@@ -754,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const P prob) {
   } else if (threadIdx.x < kTkBase) {
     bookkeeper_loop(prob, sh);
   } else if (threadIdx.x < kFinBase) {
-    ticketer_loop(prob, sh, tab);
+    if (!P::kCtrl) ticketer_loop(prob, sh, tab);  // control CTAs poll the counts themselves
   } else if (threadIdx.x < kConsBase) {
     if (P::kHasDraws && threadIdx.x >= kScBase) scout_loop(prob, sh);
     else if (!P::kCtrl) finalizer_loop(prob, sh, tab);

@@ -108,6 +108,7 @@ struct StageMeta {
   const char* src2;  // second row's chunk (residual pass), or null
   float4 aux;        // residual pass: mp, 1/Zp, mq, 1/Zq
   int sub;           // residual pass: mode
+  int slot;          // where the chunk's partial / segment sums go
 };
 
 // What the bookkeeper needs about a result slot.

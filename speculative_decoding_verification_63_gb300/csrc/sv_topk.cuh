@@ -284,6 +284,14 @@ __device__ void tk_merge(const TopkPass& a, int r, int k, Scale2 c, TkBuf& bf, i
     bf.cnt += ns;
   }
   __syncwarp();
+  // leave the row's segment lists and counts zero for the next call (any
+  // part of the workspace may serve another call's partials, which must
+  // start at zero)
+  for (int s = 0; s < a.n_seg; ++s) {
+    float2* src = a.seg_lists + (static_cast<size_t>(r) * a.n_seg + s) * a.max_topk;
+    for (int i = lane; i < a.max_topk; i += 32) src[i] = make_float2(0.f, 0.f);
+    if (lane == 0) a.seg_count[static_cast<size_t>(r) * a.n_seg + s] = 0;
+  }
   if (bf.cnt > k) tk_cut(bf, k, lane);
   __syncwarp();
   float2* out = a.lists + static_cast<size_t>(r) * a.max_topk;

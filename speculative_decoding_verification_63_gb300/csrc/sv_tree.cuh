@@ -421,6 +421,15 @@ __device__ void TreeProblem::finalize(Shared& sh, const PosTables& tab, int pos,
     if (err) record_error(&ws.hdr->error, err);
     ws.tickets[b] = 0u;
   }
+  // leave the request's chunk partials and residual rows zero: any part of
+  // the workspace may serve a later chain call's partials, which must start
+  // at zero
+  for (int i = ftid; i < nrows * ipr; i += kFinThreads)
+    ws.partials[static_cast<size_t>(r0) * ipr + i] = make_float2(0.f, 0.f);
+  if (!greedy) {
+    float* wrow = ws.scratch + static_cast<size_t>(b) * 2 * V;
+    for (int i = ftid; i < 2 * V; i += kFinThreads) wrow[i] = 0.f;
+  }
   named_sync(1, kFinThreads);
 }
 

@@ -131,6 +131,27 @@ def test_workspace_reuse_gives_same_result():
     assert st == sv.SV_OK and flags == 0
 
 
+def test_one_workspace_serves_calls_of_any_shape():
+    """Chain calls of different shapes, a tree call and a top-k call in turn
+    on one workspace: what one call writes anywhere in it must not be taken
+    by the next for its own results (the sequence B = 64, 1, 1, 1, 3 once
+    reused segment sums as chunk partials)."""
+    from gpu_util import check_tree
+    need = max(sv.sv_chain_workspace_bytes(64, 8, 32_000, sv.SV_BF16, 64),
+               sv.sv_tree_workspace_bytes(16, 32, 32, 32_000, sv.SV_BF16))
+    ws = sv.workspace(need, "cuda", "shapes")
+    check_chain(wl.make_chain(2, B=64), ws=ws)
+    for s_ in range(3):
+        check_chain(wl.make_chain(2, B=1, seed=wl.SEED_BASE + 2 + 17 * s_ + 1), ws=ws)
+    check_chain(wl.make_chain(2, B=3, seed=wl.SEED_BASE + 2 + 3), ws=ws)
+    check_tree(wl.make_tree(B=6, seed=61), ws=ws)
+    check_chain(wl.make_chain(3, B=5, V=20_000, seed=62), ws=ws)
+    check_chain(wl.make_chain(5, B=8, V=20_000, seed=wl.SEED_BASE + 563), ws=ws)
+    check_chain(wl.make_chain(2, B=3, seed=wl.SEED_BASE + 2 + 3), ws=ws)
+    st, flags = sv.sv_get_error(ws)
+    assert st == sv.SV_OK and flags == 0
+
+
 def test_data_errors_are_reported_per_request():
     inp = wl.make_chain(2, B=6, V=2000, seed=15)
     t = wl.bf16_bits_to_f32(inp["target"]).copy()
