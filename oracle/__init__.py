@@ -73,8 +73,12 @@ def _declare(lib):
     lib.svo_icdf.restype = ctypes.c_int
     lib.svo_verify_chain.argtypes = [ctypes.c_int] * 4 + [_P] * 7 + [_P] * 8
     lib.svo_verify_chain.restype = ctypes.c_int
-    lib.svo_verify_tree.argtypes = [ctypes.c_int] * 6 + [_P] * 10 + [_P] * 7
+    lib.svo_verify_tree.argtypes = [ctypes.c_int] * 7 + [_P] * 10 + [_P] * 7
     lib.svo_verify_tree.restype = ctypes.c_int
+    lib.svo_tree_mask.argtypes = [ctypes.c_int] * 3 + [_P] * 5
+    lib.svo_tree_mask.restype = ctypes.c_int
+    lib.svo_row_stats.argtypes = [ctypes.c_int] * 4 + [_P] * 8
+    lib.svo_row_stats.restype = ctypes.c_int
     return lib
 
 
@@ -177,10 +181,14 @@ def verify_chain_inputs(inp: dict, requests=None, lib=None) -> dict:
 
 # -------------------------------------------------------------------- tree
 
+TREE_MODES = {"mss": 0, "noreplace": 1, "naive": 2}
+
+
 def verify_tree(target, draft, node_tokens, parent, q_row, temperature,
                 u_accept, u_sample, num_nodes=None, top_k=None, max_depth=None,
-                lib=None) -> dict:
-    """Token-tree verification (MSS / VerifyGreedy), see svo_verify_tree."""
+                mode: str = "mss", lib=None) -> dict:
+    """Token-tree verification (VerifyGreedy, and MSS, MSS without
+    replacement or naive sampling by `mode`), see svo_verify_tree."""
     lib = lib or load()
     dt, target = _logits(target)
     dt2, draft = _logits(draft)
@@ -201,7 +209,8 @@ def verify_tree(target, draft, node_tokens, parent, q_row, temperature,
                accepted_nodes=np.zeros((B, max(max_depth, 1)), np.int32),
                margin_accept=np.zeros(B), margin_draw=np.zeros(B),
                status=np.zeros(B, np.int32))
-    lib.svo_verify_tree(B, N, M, V, dt, max_depth, _ptr(target), _ptr(draft),
+    lib.svo_verify_tree(B, N, M, V, dt, max_depth, TREE_MODES[mode], _ptr(target),
+                        _ptr(draft),
                         _ptr(node_tokens), _ptr(parent), _ptr(q_row), _ptr(nn),
                         _ptr(temperature), _ptr(tk), _ptr(u_accept), _ptr(u_sample),
                         _ptr(out["out_tokens"]), _ptr(out["out_len"]),
@@ -214,10 +223,55 @@ def verify_tree(target, draft, node_tokens, parent, q_row, temperature,
     return out
 
 
-def verify_tree_inputs(inp: dict, requests=None, lib=None) -> dict:
+def verify_tree_inputs(inp: dict, requests=None, mode: str | None = None, lib=None) -> dict:
     sel = slice(None) if requests is None else np.asarray(requests)
     return verify_tree(inp["target"][sel], inp["draft"][sel], inp["node_tokens"][sel],
                        inp["parent"][sel], inp["q_row"][sel], inp["temperature"][sel],
                        inp["u_accept"][sel], inp["u_sample"][sel],
                        num_nodes=inp["num_nodes"][sel], top_k=inp["top_k"][sel],
-                       max_depth=inp["max_depth"], lib=lib)
+                       max_depth=inp["max_depth"],
+                       mode=mode if mode is not None else inp.get("mode", "mss"), lib=lib)
+
+
+# ------------------------------------------------------- tree attention mask
+
+def tree_mask(parent, num_nodes=None, words: int | None = None, lib=None) -> dict:
+    """Ancestor bitmask rows and depths of DFS-linearised trees, see
+    svo_tree_mask.  Returns mask [B][N][words] uint32, depth [B][N], status."""
+    lib = lib or load()
+    parent = np.ascontiguousarray(parent, dtype=np.int32)
+    B, N = parent.shape
+    W = (N + 31) // 32 if words is None else words
+    nn = None if num_nodes is None else np.ascontiguousarray(num_nodes, dtype=np.int32)
+    out = dict(mask=np.zeros((B, N, W), np.uint32), depth=np.zeros((B, N), np.int32),
+               status=np.zeros(B, np.int32))
+    lib.svo_tree_mask(B, N, W, _ptr(parent), _ptr(nn), _ptr(out["mask"]),
+                      _ptr(out["depth"]), _ptr(out["status"]))
+    return out
+
+
+# --------------------------------------------------- per-position statistics
+
+def row_stats(target, draft, temperature, num_drafts=None, top_k=None, lib=None) -> dict:
+    """alpha_i = sum min(p_i, q_i) per position and the expected tokens
+    per round, see svo_row_stats."""
+    lib = lib or load()
+    dt, target = _logits(target)
+    dt2, draft = _logits(draft)
+    assert dt == dt2
+    B, R, V = target.shape
+    K = R - 1
+    assert draft.shape[:2] == (B, K)
+    nd = None if num_drafts is None else np.ascontiguousarray(num_drafts, dtype=np.int32)
+    tk = None if top_k is None else np.ascontiguousarray(top_k, dtype=np.int32)
+    temperature = np.ascontiguousarray(temperature, dtype=np.float32)
+    out = dict(alpha=np.zeros((B, K)), expected=np.zeros(B), status=np.zeros(B, np.int32))
+    lib.svo_row_stats(B, K, V, dt, _ptr(target), _ptr(draft), _ptr(nd), _ptr(temperature),
+                      _ptr(tk), _ptr(out["alpha"]), _ptr(out["expected"]),
+                      _ptr(out["status"]))
+    return out
+
+
+def row_stats_inputs(inp: dict, lib=None) -> dict:
+    return row_stats(inp["target"], inp["draft"], inp["temperature"],
+                     num_drafts=inp["num_drafts"], top_k=inp["top_k"], lib=lib)

@@ -357,11 +357,33 @@ int svo_verify_chain(int B, int K, int V, int dtype, const void* target,
  * draw from r.  A node without children: draw from p_node (bonus).
  * Greedy: go to the first child whose token is argmax p_node, else emit it.
  *
+ * mode selects the stochastic rule (greedy walks are the same in every mode):
+ *   SVO_TREE_MSS (0)   as above; the children are assumed drawn i.i.d. from
+ *                      their q ([L17] sec. 4.5, the precondition of Thm 4.2).
+ *   SVO_TREE_NOREPLACE (1)  multi-step speculative sampling for children
+ *                      drawn WITHOUT replacement ([L17] sec. 4.5, the remark
+ *                      on the proof's precondition, and sec. 10 exercise 7,
+ *                      the unbiased fix): the j-th child tried at a node is
+ *                      tested, and the residual formed, with q_j = q with
+ *                      the tokens of the siblings tried before it set to 0,
+ *                      renormalised (q = the child's own draft row).  A q_j
+ *                      of zero mass is all zero (its child is accepted iff
+ *                      r(x) > 0, and a rejection leaves r unchanged).
+ *   SVO_TREE_NAIVE (2) naive sampling ([L17] sec. 4.5): at the current node
+ *                      draw x from p_node by inverse CDF with the node's own
+ *                      uniform u_accept[node]; move to the first child whose
+ *                      token is x, else emit x.  u_sample is unused, and
+ *                      margin_draw is the smallest margin over the draws.
+ *
  * Outputs: out_tokens [B][max_depth+1], accepted_nodes [B][max_depth]
  * (-1 padded), out_len, accept_len, margin_accept, margin_draw, status as
  * for the chain.
  */
-int svo_verify_tree(int B, int N, int M, int V, int dtype, int max_depth,
+#define SVO_TREE_MSS 0
+#define SVO_TREE_NOREPLACE 1
+#define SVO_TREE_NAIVE 2
+
+int svo_verify_tree(int B, int N, int M, int V, int dtype, int max_depth, int mode,
                     const void* target, const void* draft,
                     const int* node_tokens, const int* parent,
                     const int* q_row, const int* num_nodes,
@@ -376,6 +398,7 @@ int svo_verify_tree(int B, int N, int M, int V, int dtype, int max_depth,
   double* q = (double*)malloc(sizeof(double) * (size_t)V);
   double* w = (double*)malloc(sizeof(double) * (size_t)V);
   int* depth = (int*)malloc(sizeof(int) * (size_t)(N > 0 ? N : 1));
+  int* tried = (int*)malloc(sizeof(int) * (size_t)(N > 0 ? N : 1));
   int n_err = 0;
   for (int b = 0; b < B; ++b) {
     const char* trow0 = (const char*)target + (size_t)b * N * V * es;
@@ -398,7 +421,7 @@ int svo_verify_tree(int B, int N, int M, int V, int dtype, int max_depth,
     status[b] = SVO_OK;
 
     int st = SVO_OK;
-    if (nn < 1 || nn > N || !(T >= 0.0)) st = SVO_EARG;
+    if (nn < 1 || nn > N || !(T >= 0.0) || mode < 0 || mode > 2) st = SVO_EARG;
     else if (par[0] != -1) st = SVO_ETREE;
     if (st == SVO_OK) depth[0] = 0;
     for (int n = 1; st == SVO_OK && n < nn; ++n) {
@@ -427,6 +450,21 @@ int svo_verify_tree(int B, int N, int M, int V, int dtype, int max_depth,
         node = next;
         continue;
       }
+      if (mode == SVO_TREE_NAIVE) {
+        double mgn = INFINITY;
+        int x = svo_icdf(p, V, (double)ua[node], &mgn);
+        if (mgn < margin_draw[b]) margin_draw[b] = mgn;
+        if (x < 0) { token = -1; break; }
+        int next = -1;
+        for (int c = node + 1; c < nn; ++c)
+          if (par[c] == node && tok[c] == x) { next = c; break; }
+        if (next < 0) { token = x; break; }
+        out[L] = x;
+        acc[L] = next;
+        ++L;
+        node = next;
+        continue;
+      }
       int has_child = 0;
       for (int c = node + 1; c < nn; ++c)
         if (par[c] == node) { has_child = 1; break; }
@@ -437,12 +475,21 @@ int svo_verify_tree(int B, int N, int M, int V, int dtype, int max_depth,
         break;
       }
       memcpy(r, p, sizeof(double) * (size_t)V);
-      int next = -1;
+      int next = -1, n_tried = 0;
       for (int c = node + 1; c < nn && st == SVO_OK; ++c) {
         if (par[c] != node) continue;
         st = svo_row_probs(drow0 + (size_t)qr[c] * V * es, dtype, V, T, tk, q);
         if (st != SVO_OK) break;
+        if (mode == SVO_TREE_NOREPLACE) {
+          /* q_j: the earlier-tried siblings' tokens removed, renormalised */
+          for (int j = 0; j < n_tried; ++j) q[tried[j]] = 0.0;
+          double sq = 0.0;
+          for (int t = 0; t < V; ++t) sq += q[t];
+          if (sq > 0.0)
+            for (int t = 0; t < V; ++t) q[t] /= sq;
+        }
         int xc = tok[c];
+        tried[n_tried++] = xc;
         double m1 = accept_margin((double)ua[c], q[xc], r[xc]);
         if (m1 < margin_accept[b]) margin_accept[b] = m1;
         if ((double)ua[c] * q[xc] < r[xc]) { next = c; break; }
@@ -479,5 +526,111 @@ int svo_verify_tree(int B, int N, int M, int V, int dtype, int max_depth,
   free(q);
   free(w);
   free(depth);
+  free(tried);
+  return n_err;
+}
+
+/* ------------------------------------------------- tree attention mask */
+
+/*
+ * Topology-aware causal mask and depth position ids of a depth-first
+ * linearised token tree ([L17] sec. 4.3, tree attention: a node attends to
+ * the verified prefix, its ancestors and itself; positions are given by
+ * depth, so nodes at the same depth share one; sec. 10 exercise 5).
+ *
+ * Request b has n = num_nodes[b] nodes (num_nodes NULL: N), node 0 the root,
+ * parent[0] == -1 and 0 <= parent[i] < i.  mask [B][N][W] (W >= ceil(N/32)
+ * 32-bit words per row): bit (j % 32) of word j / 32 of row i is set iff j is
+ * i or an ancestor of i.  depth [B][N]: edges from the root.  Rows i >= n and
+ * every row of a malformed request are zero with depth -1; a malformed
+ * request gets status SVO_ETREE (SVO_EARG for n outside [1, N]).
+ */
+int svo_tree_mask(int B, int N, int W, const int* parent, const int* num_nodes,
+                  uint32_t* mask, int* depth, int* status) {
+  int n_err = 0;
+  for (int b = 0; b < B; ++b) {
+    const int* par = parent + (size_t)b * N;
+    uint32_t* mrow = mask + (size_t)b * N * W;
+    int* dep = depth + (size_t)b * N;
+    int n = num_nodes ? num_nodes[b] : N;
+    for (int i = 0; i < N * W; ++i) mrow[i] = 0u;
+    for (int i = 0; i < N; ++i) dep[i] = -1;
+    int st = SVO_OK;
+    if (n < 1 || n > N) st = SVO_EARG;
+    else if (par[0] != -1) st = SVO_ETREE;
+    for (int i = 1; st == SVO_OK && i < n; ++i)
+      if (par[i] < 0 || par[i] >= i) st = SVO_ETREE;
+    status[b] = st;
+    if (st != SVO_OK) { ++n_err; continue; }
+    for (int i = 0; i < n; ++i) {
+      int d = -1;
+      for (int j = i; j >= 0; j = (j == 0 ? -1 : par[j])) {
+        mrow[(size_t)i * W + j / 32] |= 1u << (j % 32);
+        ++d;
+      }
+      dep[i] = d;
+    }
+  }
+  return n_err;
+}
+
+/* ------------------------------------------------- per-position statistics */
+
+/*
+ * Acceptance statistics of a chain round ([L17] sec. 2.3, Thm 3.5: the
+ * acceptance rate of position i is alpha_i = sum_x min(p_i(x), q_i(x)) =
+ * 1 - TV(p_i, q_i); [N02] sec. 7: E[N] = (1 - a^(K+1)) / (1 - a) for i.i.d.
+ * acceptance; the per-position form sum_{j=0..nd} prod_{i<j} alpha_i, which
+ * reduces to it when every alpha_i = a).
+ *
+ * For request b with nd = num_drafts[b] (NULL: K) and every position
+ * i < nd: p_i, q_i = svo_row_probs of target row i and draft row i (greedy:
+ * one-hot argmax, so alpha_i is 1 iff the argmaxes agree); alpha [B][K]
+ * (NaN at i >= nd); expected [B] = sum_{j=0..nd} prod_{i<j} alpha_i, the
+ * expected number of tokens the round emits.  A request with a data error
+ * gets NaN everywhere and its status.
+ */
+int svo_row_stats(int B, int K, int V, int dtype, const void* target, const void* draft,
+                  const int* num_drafts, const float* temperature, const int* top_k,
+                  double* alpha, double* expected, int* status) {
+  const size_t es = dtype == 0 ? 2 : 4;
+  double* p = (double*)malloc(sizeof(double) * (size_t)V);
+  double* q = (double*)malloc(sizeof(double) * (size_t)V);
+  int n_err = 0;
+  for (int b = 0; b < B; ++b) {
+    int nd = num_drafts ? num_drafts[b] : K;
+    double T = (double)temperature[b];
+    int tk = top_k ? top_k[b] : 0;
+    double* al = alpha + (size_t)b * K;
+    for (int i = 0; i < K; ++i) al[i] = NAN;
+    expected[b] = NAN;
+    int st = SVO_OK;
+    if (nd < 0 || nd > K || !(T >= 0.0) || tk < 0) st = SVO_EARG;
+    for (int i = 0; st == SVO_OK && i < nd; ++i) {
+      st = svo_row_probs((const char*)target + ((size_t)b * (K + 1) + i) * V * es, dtype, V,
+                         T, tk, p);
+      if (st != SVO_OK) break;
+      st = svo_row_probs((const char*)draft + ((size_t)b * K + i) * V * es, dtype, V, T,
+                         tk, q);
+      if (st != SVO_OK) break;
+      double a = 0.0;
+      for (int t = 0; t < V; ++t) a += p[t] < q[t] ? p[t] : q[t];
+      al[i] = a;
+    }
+    status[b] = st;
+    if (st != SVO_OK) {
+      for (int i = 0; i < K; ++i) al[i] = NAN;
+      ++n_err;
+      continue;
+    }
+    double e = 0.0, reach = 1.0;
+    for (int j = 0; j <= nd; ++j) {
+      e += reach;
+      if (j < nd) reach *= al[j];
+    }
+    expected[b] = e;
+  }
+  free(p);
+  free(q);
   return n_err;
 }

@@ -220,7 +220,8 @@ def make_tree(seed: int | None = None, B: int | None = None,
               N: int | None = None, V: int | None = None,
               max_depth: int | None = None, max_branch: int | None = None,
               temperature: float = 0.8, greedy_hint: float = 0.0,
-              dtype: str | None = None, nodes_min: int | None = None) -> dict:
+              dtype: str | None = None, nodes_min: int | None = None,
+              replace: bool = True) -> dict:
     """Seeded inputs for the token-tree workload (4).
 
     Each request gets a random tree (see random_tree_shape) with between
@@ -228,9 +229,12 @@ def make_tree(seed: int | None = None, B: int | None = None,
     distribution after the path root..n; draft row m is the draft
     distribution at node m, used by the children of m (q_row[n] =
     parent[n]).  Children tokens are drawn i.i.d. from the parent's draft
-    distribution.  With greedy_hint > 0 (greedy trees), the first child of a
-    node takes the argmax of the node's target row with that probability, so
-    greedy walks go deep.
+    distribution: i.i.d. (replace=True), or without replacement among the
+    children of one node (replace=False: each child is drawn from the draft
+    distribution with its earlier siblings' tokens excluded).  With
+    greedy_hint > 0 (greedy trees), the first child of a node takes the
+    argmax of the node's target row with that probability, so greedy walks
+    go deep.
     """
     sh = TREE_SHAPE
     B = sh["B"] if B is None else B
@@ -264,14 +268,20 @@ def make_tree(seed: int | None = None, B: int | None = None,
         parent[b, :n_b] = par
         q_row[b, 1:n_b] = par[1:]
         first_child_seen = set()
+        used: dict[int, set] = {}
         for n in range(1, n_b):
             u = int(par[n])
             if (greedy_hint > 0.0 and u not in first_child_seen
                     and rng.random() < greedy_hint):
                 tokens[b, n] = int(np.argmax(t_vals[b, u].astype(np.float64)))
             else:
-                tokens[b, n] = draw_draft(rng, d_vals[b, u], float(temperature))
+                row = d_vals[b, u]
+                if not replace and used.get(u):
+                    row = row.astype(np.float64)
+                    row[sorted(used[u])] = -np.inf
+                tokens[b, n] = draw_draft(rng, row, float(temperature))
             first_child_seen.add(u)
+            used.setdefault(u, set()).add(int(tokens[b, n]))
     u_acc = uniforms(rng, (B, N))
     u_smp = uniforms(rng, (B,))
     return dict(target=_pack(t_logits, dtype), draft=_pack(d_logits, dtype),
@@ -279,7 +289,7 @@ def make_tree(seed: int | None = None, B: int | None = None,
                 num_nodes=num_nodes, temperature=temp,
                 top_k=np.zeros(B, dtype=np.int32), u_accept=u_acc,
                 u_sample=u_smp, dtype=dtype, B=B, N=N, M=N, V=V,
-                max_depth=max_depth)
+                max_depth=max_depth, mode="mss" if replace else "noreplace")
 
 
 def chain_algorithmic_bytes(inp: dict) -> int:

@@ -601,3 +601,307 @@ ALL_FAST = [check_worked_round_n02_sec9, check_exercise2_n02, check_residual_lem
             check_deterministic_draft_bias]
 ALL_MC = [check_mc_chain, check_mc_expected_tokens, check_mc_temperature_topk,
           check_mc_toy_sequences, check_tree_mc_lossless, check_tree_deeper_mc]
+
+
+# ---------------------------------------- tree: MSS without replacement, naive
+
+def _one_level_tree(p, q, child_tokens, ua_children, us=0.5, mode="mss", lib=None):
+    """Root with children proposing child_tokens, all from the one draft row q."""
+    V = len(p)
+    n = 1 + len(child_tokens)
+    t = np.zeros((1, n, V), np.float32)
+    t[0, 0] = logits_of(p)
+    d = logits_of(q)[None, None]
+    tok = np.array([[0] + list(child_tokens)], np.int32)
+    par = np.array([[-1] + [0] * len(child_tokens)], np.int32)
+    qr = np.zeros((1, n), np.int32)
+    ua = np.array([[0.0] + list(ua_children)], np.float32)
+    return oracle.verify_tree(t, d, tok, par, qr, [1.0], ua, [us], max_depth=1,
+                              mode=mode, lib=lib)
+
+
+def check_tree_noreplace_thresholds(lib):
+    """[L17] sec. 4.5 (the MSS proof needs the j-th draft to be drawn from
+    q_j) and sec. 10 exercise 7 (the fix: children drawn without replacement,
+    the j-th tested against q with the earlier tokens removed, renormalised).
+
+    p = (.2, .5, .3), q = (.5, .25, .25); children propose token 0 then
+    token 2.  Token 0 is rejected for u >= p(0)/q(0) = 0.4; the residual is
+    max(0, p - q) / 0.3 = (0, 5/6, 1/6).  Token 2 is then tested against
+    q_1 = (0, .5, .5) without replacement (threshold (1/6)/0.5 = 1/3), and
+    against q = (.5, .25, .25) with replacement (threshold (1/6)/0.25 = 2/3).
+    After a rejection of token 2, max(0, r - q_1) = (0, 1/3, 0): the draw is
+    token 1 whatever u_sample is."""
+    p, q = [0.2, 0.5, 0.3], [0.5, 0.25, 0.25]
+    cases = [  # (u for child 0, u for child 1) -> accepted node per mode
+        ((0.39, 0.9), 1, 1),
+        ((0.41, 0.30), 2, 2),
+        ((0.9, 0.34), 2, 0),   # accepted with replacement only
+        ((0.9, 0.66), 2, 0),
+        ((0.9, 0.68), 0, 0),
+    ]
+    for ua, mss_node, nor_node in cases:
+        for mode, want in (("mss", mss_node), ("noreplace", nor_node)):
+            for us in (0.01, 0.5, 0.999):
+                out = _one_level_tree(p, q, [0, 2], ua, us=us, mode=mode, lib=lib)
+                assert out["status"][0] == 0
+                got = int(out["accepted_nodes"][0][0]) if out["accept_len"][0] else 0
+                assert got == want, (mode, ua, got)
+                if want == 0 and mode == "noreplace":
+                    assert out["out_tokens"][0][0] == 1, out  # residual (0, 1, 0)
+    # the removed token can no longer be accepted: a third child repeating
+    # token 0 has q_2(0) = 0 and r(0) = 0
+    out = _one_level_tree(p, q, [0, 2, 0], (0.9, 0.9, 0.0), mode="noreplace", lib=lib)
+    assert out["accept_len"][0] == 0 and out["out_tokens"][0][0] == 1
+
+
+def check_tree_noreplace_mc_lossless(lib, n=120_000, seed=34):
+    """Children drawn without replacement from one q, tested with the
+    renormalised q_j: the emitted first token still follows p_root (the
+    unbiased fix of [L17] sec. 10 exercise 7), at the accept rate the exact
+    enumeration gives."""
+    rng = np.random.default_rng(seed)
+    V = 5
+    p = rng.dirichlet(np.ones(V))
+    q = rng.dirichlet(np.ones(V) * 0.7)
+    ex = en.mss_exact(p, [q] * 3, mode="without_replacement")
+    assert np.abs(ex["emitted"] - p).max() < 1e-12
+    N = 4
+    t = np.zeros((n, N, V), np.float32)
+    t[:, 0] = logits_of(p)
+    d = np.broadcast_to(logits_of(q)[None, None], (n, 1, V))
+    # sequential sampling without replacement: Gumbel top-3 of log q
+    g = np.log(q)[None] + rng.gumbel(size=(n, V))
+    order = np.argsort(-g, axis=1)[:, :3].astype(np.int32)
+    tok = np.concatenate([np.zeros((n, 1), np.int32), order], 1)
+    par = np.tile(np.array([-1, 0, 0, 0], np.int32), (n, 1))
+    qr = np.zeros((n, N), np.int32)
+    ua = rng.random((n, N)).astype(np.float32)
+    us = rng.random(n).astype(np.float32)
+    out = oracle.verify_tree(t, d, tok, par, qr, np.ones(n), ua, us, max_depth=1,
+                             mode="noreplace", lib=lib)
+    assert np.all(out["status"] == 0)
+    assert chi2_ok(np.bincount(out["out_tokens"][:, 0], minlength=V), p)
+    acc = (out["accept_len"] == 1).mean()
+    assert abs(acc - ex["accept"]) < 5 * np.sqrt(ex["accept"] * (1 - ex["accept"]) / n)
+
+
+def check_tree_naive_examples(lib):
+    """[L17] sec. 4.5 slides example and sec. 10 exercise 6: naive sampling
+    draws from p (uniform on 4 tokens) and accepts when the draw is a child's
+    token: 50 % in both.  The draw is the inverse CDF of p at the root's
+    uniform, so over an even grid of u exactly half the points accept."""
+    for key in ("slides_example", "exercise6"):
+        g = golden("l17_exercises.json")[key]
+        want = g.get("naive_accept_this_draw", g.get("naive_accept"))
+        kids = [g["draft1"], g["draft2"]]
+        hits = 0
+        G = 64
+        for k in range(G):
+            u = (k + 0.5) / G
+            t, d, tok, par, qr = _tree_inputs(g["p"], [g["q1"], g["q2"]], kids, 4)
+            out = oracle.verify_tree(t, d, tok, par, qr, [1.0], [[u, 0.3, 0.3]], [0.5],
+                                     max_depth=1, mode="naive", lib=lib)
+            assert out["status"][0] == 0
+            x = int(k * 4 // G)  # inverse CDF of the uniform p
+            if x in kids:
+                hits += 1
+                assert out["accept_len"][0] == 1
+                assert out["accepted_nodes"][0][0] == 1 + kids.index(x)
+                assert out["out_tokens"][0][0] == x
+            else:
+                assert out["accept_len"][0] == 0 and out["out_tokens"][0][0] == x
+        assert hits / G == want, (key, hits)
+
+
+def check_tree_naive_mc(lib, n=100_000, seed=35):
+    """Naive sampling is lossless (it only ever emits draws from p) and, on
+    the same inputs, accepts no more often than MSS (Theorem 4.3); its rate
+    matches the exact enumeration's naive rate."""
+    rng = np.random.default_rng(seed)
+    V = 5
+    p = rng.dirichlet(np.ones(V))
+    qs = [rng.dirichlet(np.ones(V)) for _ in range(3)]
+    ex = en.mss_exact(p, qs)
+    N = 4
+    t = np.zeros((n, N, V), np.float32)
+    t[:, 0] = logits_of(p)
+    d = np.broadcast_to(np.stack([logits_of(q) for q in qs])[None], (n, 3, V))
+    tok = np.zeros((n, N), np.int32)
+    for j in range(3):
+        tok[:, j + 1] = rng.choice(V, n, p=qs[j])
+    par = np.tile(np.array([-1, 0, 0, 0], np.int32), (n, 1))
+    qr = np.tile(np.array([0, 0, 1, 2], np.int32), (n, 1))
+    ua = rng.random((n, N)).astype(np.float32)
+    us = rng.random(n).astype(np.float32)
+    nv = oracle.verify_tree(t, d, tok, par, qr, np.ones(n), ua, us, max_depth=1,
+                            mode="naive", lib=lib)
+    ms = oracle.verify_tree(t, d, tok, par, qr, np.ones(n), ua, us, max_depth=1, lib=lib)
+    assert np.all(nv["status"] == 0)
+    assert chi2_ok(np.bincount(nv["out_tokens"][:, 0], minlength=V), p)
+    a_nv = (nv["accept_len"] == 1).mean()
+    a_ms = (ms["accept_len"] == 1).mean()
+    sd = np.sqrt(0.25 / n)
+    assert abs(a_nv - ex["naive_accept"]) < 5 * sd
+    assert a_ms >= a_nv - 5 * sd and abs(a_ms - ex["accept"]) < 5 * sd
+
+
+def check_tree_modes_agree_when_greedy(lib):
+    """VerifyGreedy ([L17] sec. 4.4) does not depend on the stochastic rule."""
+    rng = np.random.default_rng(36)
+    B, N, V = 30, 9, 7
+    t = rng.normal(0, 2, (B, N, V)).astype(np.float32)
+    d = rng.normal(0, 2, (B, N, V)).astype(np.float32)
+    par = np.tile(np.array([-1, 0, 1, 1, 0, 4, 4, 6, 0], np.int32), (B, 1))
+    tok = rng.integers(0, V, (B, N)).astype(np.int32)
+    ua = rng.random((B, N)).astype(np.float32)
+    us = rng.random(B).astype(np.float32)
+    outs = [oracle.verify_tree(t, d, tok, par, np.maximum(par, 0), np.zeros(B), ua, us,
+                               max_depth=3, mode=m, lib=lib)
+            for m in ("mss", "noreplace", "naive")]
+    for o in outs[1:]:
+        assert np.array_equal(o["out_tokens"], outs[0]["out_tokens"])
+
+
+# ------------------------------------------------------- tree attention mask
+
+def check_tree_mask_slides(lib):
+    """[L17] sec. 4.3: the slides' mask (machine / learning / algorithm /
+    system / design / translation / model) and sec. 10 exercise 5 (what e
+    sees; depths as position offsets)."""
+    g = golden("l17_tree_mask.json")
+    names = g["nodes"]
+    parent_name = {"machine": None, "learning": "machine", "algorithm": "learning",
+                   "system": "learning", "design": "system", "translation": "machine",
+                   "model": "translation"}
+    # node 0 is the verified root; the speculated tokens follow in the
+    # order the slides list them (a depth-first order)
+    par = [-1] + [0 if parent_name[x] is None else 1 + names.index(parent_name[x])
+                  for x in names]
+    out = oracle.tree_mask(np.array([par], np.int32), lib=lib)
+    assert out["status"][0] == 0
+    m = out["mask"][0][:, 0]
+    for i, row in enumerate(g["visible"]):
+        want = {0} | {1 + names.index(x) for x in row}
+        got = {j for j in range(len(par)) if (m[1 + i] >> j) & 1}
+        assert got == want, (names[i], got, want)
+    e5 = golden("l17_ex5_tree.json")
+    out = oracle.tree_mask(np.array([e5["parent"]], np.int32), lib=lib)
+    assert list(out["depth"][0]) == e5["depth"]
+    sees = {e5["dfs_order"][j] for j in range(8) if (out["mask"][0][5][0] >> j) & 1}
+    assert sees == set(e5["ancestors_of_e"]) | {"e"}
+
+
+def check_tree_mask_closure(lib):
+    """Random DFS trees (up to 64 nodes, two mask words): the mask is the
+    reflexive-transitive closure of the parent relation (boolean matrix
+    powers) and the depth is the number of proper ancestors; malformed
+    trees and padding rows come back empty."""
+    rng = np.random.default_rng(37)
+    B, N = 40, 64
+    par = np.full((B, N), -1, np.int32)
+    nn = rng.integers(1, N + 1, B).astype(np.int32)
+    for b in range(B):
+        for i in range(1, nn[b]):
+            par[b, i] = rng.integers(max(0, i - 5), i)  # a parent shortly before
+    bad = 3
+    par[bad, 7] = 7 if nn[bad] > 7 else par[bad, 7]
+    nn[bad] = max(nn[bad], 8)
+    out = oracle.tree_mask(par, nn, lib=lib)
+    for b in range(B):
+        if b == bad:
+            assert out["status"][b] != 0 and not out["mask"][b].any()
+            assert np.all(out["depth"][b] == -1)
+            continue
+        n = nn[b]
+        A = np.zeros((n, n), bool)
+        for i in range(1, n):
+            A[i, par[b, i]] = True
+        R = np.eye(n, dtype=bool)
+        step = np.eye(n, dtype=bool)
+        for _ in range(n):
+            step = (step.astype(int) @ A.astype(int)) > 0
+            R |= step
+        bits = np.zeros((N, 64), bool)
+        words = out["mask"][b]
+        for w in range(2):
+            for k in range(32):
+                bits[:, 32 * w + k] = (words[:, w] >> np.uint32(k)) & 1
+        assert np.array_equal(bits[:n, :n], R), b
+        assert not bits[:n, n:].any() and not bits[n:].any()
+        assert np.array_equal(out["depth"][b][:n], R.sum(1) - 1)
+        assert np.all(out["depth"][b][n:] == -1)
+
+
+# -------------------------------------------------- per-position statistics
+
+def check_row_stats_worked(lib):
+    """[N02] sec. 9: q = (.5, .2, .15, .1, .05), p = (.3, .35, .2, .1, .05)
+    gives alpha = 0.8, and with three such positions E[N] = 2.952; the
+    printed E[tokens] examples for identical positions; p == q accepts
+    everything (E[N] = K + 1)."""
+    g = golden("n02_sec9_worked_round.json")
+    p, q = np.array(g["p"]), np.array(g["q"])
+    K = 3
+    t = np.tile(logits_of(p), (1, K + 1, 1)).astype(np.float32)
+    d = np.tile(logits_of(q), (1, K, 1)).astype(np.float32)
+    out = oracle.row_stats(t, d, [1.0], lib=lib)
+    assert np.allclose(out["alpha"][0], 0.8, atol=1e-6)
+    assert abs(out["expected"][0] - 2.952) < 1e-5
+    for ex in golden("l17_exercises.json")["E_examples"]:
+        a = ex["alpha"]
+        pp = np.array([a, 1 - a])
+        qq = np.array([1.0, 0.0])  # sum min = a
+        t = np.tile(logits_of(pp), (1, ex["K"] + 1, 1)).astype(np.float32)
+        with np.errstate(divide="ignore"):
+            d = np.tile(np.log(qq), (1, ex["K"], 1)).astype(np.float32)
+        out = oracle.row_stats(t, d, [1.0], lib=lib)
+        assert round(out["expected"][0], ex["digits"]) == ex["E"], ex
+    r = np.random.default_rng(38).normal(0, 2, (2, 5, 9)).astype(np.float32)
+    out = oracle.row_stats(r, r[:, :4].copy(), [0.7, 0.0], lib=lib)
+    assert np.allclose(out["alpha"], 1.0) and np.allclose(out["expected"], 5.0)
+
+
+def check_row_stats_tv(lib):
+    """alpha = 1 - TV(p, q) (Thm 3.5) on random rows with temperature, top-k
+    and ragged drafts: TV from a library softmax; greedy positions give the
+    argmax-agreement indicator; positions past num_drafts are NaN."""
+    rng = np.random.default_rng(39)
+    B, K, V = 12, 4, 33
+    t = rng.normal(0, 2, (B, K + 1, V)).astype(np.float32)
+    d = (t[:, :K] + rng.normal(0, 1.5, (B, K, V))).astype(np.float32)
+    temp = rng.choice([0.0, 0.5, 1.0, 1.6], B).astype(np.float32)
+    nd = rng.integers(0, K + 1, B).astype(np.int32)
+    tk = rng.choice([0, 5], B).astype(np.int32)
+    out = oracle.row_stats(t, d, temp, num_drafts=nd, top_k=tk, lib=lib)
+    for b in range(B):
+        e, reach = 0.0, 1.0
+        for i in range(K):
+            a = out["alpha"][b, i]
+            if i >= nd[b]:
+                assert np.isnan(a)
+                continue
+            if temp[b] == 0:
+                want = float(np.argmax(t[b, i]) == np.argmax(d[b, i]))
+            else:
+                def dist(l):
+                    y = l.astype(np.float64) / temp[b]
+                    if tk[b]:
+                        keep = np.lexsort((np.arange(V), -y))[:tk[b]]
+                        z = np.full(V, -np.inf)
+                        z[keep] = y[keep]
+                        y = z
+                    return softmax(y)
+                want = 1.0 - 0.5 * np.abs(dist(t[b, i]) - dist(d[b, i])).sum()
+            assert abs(a - want) < 1e-12, (b, i, a, want)
+        for j in range(nd[b] + 1):
+            e += reach
+            if j < nd[b]:
+                reach *= out["alpha"][b, j]
+        assert abs(out["expected"][b] - e) < 1e-12
+
+
+ALL_FAST += [check_tree_noreplace_thresholds, check_tree_naive_examples,
+             check_tree_modes_agree_when_greedy, check_tree_mask_slides,
+             check_tree_mask_closure, check_row_stats_worked, check_row_stats_tv]
+ALL_MC += [check_tree_noreplace_mc_lossless, check_tree_naive_mc]

@@ -40,6 +40,20 @@ MUTANTS = {
         "          svo_row_probs(drow0 + (size_t)(nd - 1) * V * es, dtype, V, T, tk, q);\n"
         "          token = svo_icdf(nd > 0 ? q : p, V, (double)u[K], &mg);"),
     "greedy_emits_draft": ("      token = a[n];", "      token = n < nd ? x[n] : a[n];"),
+    "noreplace_keeps_tried": ("for (int j = 0; j < n_tried; ++j) q[tried[j]] = 0.0;",
+                              "for (int j = 0; j < n_tried; ++j) q[tried[j]] = q[tried[j]];"),
+    "noreplace_not_renormalised": ("for (int t = 0; t < V; ++t) q[t] /= sq;",
+                                   "for (int t = 0; t < V; ++t) q[t] = q[t];"),
+    "naive_takes_any_child": ("if (par[c] == node && tok[c] == x) { next = c; break; }",
+                              "if (par[c] == node) { next = c; break; }"),
+    "naive_draws_with_u_sample": ("int x = svo_icdf(p, V, (double)ua[node], &mgn);",
+                                  "int x = svo_icdf(p, V, (double)u_sample[b], &mgn);"),
+    "mask_drops_self": ("mrow[(size_t)i * W + j / 32] |= 1u << (j % 32);",
+                        "if (j != i) mrow[(size_t)i * W + j / 32] |= 1u << (j % 32);"),
+    "mask_depth_off_by_one": ("      int d = -1;", "      int d = 0;"),
+    "stats_sum_of_max": ("a += p[t] < q[t] ? p[t] : q[t];", "a += p[t] > q[t] ? p[t] : q[t];"),
+    "stats_expected_stops_early": ("for (int j = 0; j <= nd; ++j) {",
+                                   "for (int j = 0; j < nd; ++j) {"),
 }
 
 
