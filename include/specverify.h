@@ -63,8 +63,20 @@ typedef enum { SV_BF16 = 0, SV_FP32 = 1 } sv_dtype;
 
 typedef enum {
   /* SpecInfer multi-step speculative sampling: child c is tested against
-     the draft row q_row[c] as given ([L17] sec. 4.5). */
-  SV_TREE_MSS = 0
+     the draft row q_row[c] as given ([L17] sec. 4.5).  Lossless when the
+     children were drawn i.i.d. from their draft rows. */
+  SV_TREE_MSS = 0,
+  /* MSS for children drawn WITHOUT replacement ([L17] sec. 4.5, the
+     precondition of the proof, and sec. 10 exercise 7, the fix): the j-th
+     child tried at a node is tested, and the residual formed, against
+     q_j = q_row[c] with the tokens of the siblings tried before it removed
+     and renormalised; a q_j with no mass left is zero everywhere. */
+  SV_TREE_MSS_NOREPLACE = 1,
+  /* Naive sampling ([L17] sec. 4.5), the baseline MSS improves on: at the
+     current node draw x from p_node by inverse CDF with u_accept[node];
+     move to the first child whose token is x, else emit x.  Draft rows are
+     not read (draft_logits may be NULL) and u_sample is unused. */
+  SV_TREE_NAIVE = 2
 } sv_tree_mode;
 
 /* Device error flags, OR-ed into the workspace error word. */
@@ -195,6 +207,64 @@ sv_status sv_verify_chain(const sv_chain_args* args, void* workspace,
                           size_t ws_bytes, sv_stream_t stream);
 sv_status sv_verify_tree(const sv_tree_args* args, void* workspace,
                          size_t ws_bytes, sv_stream_t stream);
+
+/*
+ * Tree-attention mask and depth position ids ([L17] sec. 4.3, tree
+ * attention: the tree is laid out depth first; a node attends to the
+ * verified prefix, its ancestors and itself; a node's position is its
+ * depth; sec. 10 exercise 5).  The step that comes before the tree is
+ * verified: the target model's forward pass over the tree uses them.
+ *
+ * Request b holds n = num_nodes[b] nodes (NULL: N) in depth-first order
+ * with parent[b][0] == -1 and 0 <= parent[b][i] < i.  Outputs, row i of
+ * request b:
+ *   mask[(b*N + i)*words + j/32] bit j%32 is set iff node j is node i or
+ *   one of its ancestors (j < N; words beyond the second are zero);
+ *   depth[b*N + i] = edges from the root (the position offset after the
+ *   verified prefix).
+ * Rows i >= n are zero with depth -1.  A malformed tree records
+ * SV_DERR_TREE (n outside [1, N]: SV_DERR_ARG) and all its rows are zero
+ * with depth -1.  Only the workspace's error word is used: any workspace of
+ * at least SV_MIN_WORKSPACE_BYTES (zeroed by sv_workspace_init) will do.
+ */
+#define SV_MIN_WORKSPACE_BYTES 8192u
+
+typedef struct {
+  int32_t B, N;               /* B <= SV_MAX_TREE_B, 1 <= N <= SV_MAX_TREE_NODES */
+  int32_t words;              /* 32-bit words per mask row, >= (N + 31) / 32 */
+  const int32_t* parent;      /* [B][N] */
+  const int32_t* num_nodes;   /* [B] in [1, N], or NULL (= N) */
+  uint32_t* mask;             /* [B][N][words] */
+  int32_t* depth;             /* [B][N] */
+} sv_tree_mask_args;
+
+sv_status sv_tree_mask(const sv_tree_mask_args* args, void* workspace, size_t ws_bytes,
+                       sv_stream_t stream);
+
+/*
+ * Per-position acceptance statistics of a chain round ([L17] sec. 2.3,
+ * Thm 3.5: the draft at position i is accepted with probability
+ * alpha_i = sum_x min(p_i(x), q_i(x)) = 1 - TV(p_i, q_i); [N02] sec. 7:
+ * E[N] = (1 - a^(K+1)) / (1 - a) when every alpha_i = a).  The inputs an
+ * adaptive draft length or an on/off switch for speculation would use.
+ *
+ * Reads the target, draft, num_drafts, temperature and top_k fields of a
+ * chain call's arguments (B, K, V, dtype and strides as there; tokens,
+ * uniforms and the outputs are not used and may be NULL).  Outputs:
+ *   alpha [B][K]: alpha_i for i < num_drafts[b], NaN beyond.  Greedy
+ *     requests (t == 0) have one-hot p and q: alpha_i = 1 iff argmax p_i ==
+ *     argmax q_i (lowest id on ties), else 0.
+ *   expected [B]: sum_{j=0..nd} prod_{i<j} alpha_i, the expected number of
+ *     tokens the round emits under these rates.
+ * A request with top-k filtering (0 < top_k < V) is not supported here and
+ * is reported as SV_DERR_ARG, like a bad num_drafts or temperature; NaN or
+ * +inf logits give SV_DERR_NONFINITE, a row without mass SV_DERR_MASS.
+ * The failing request gets NaN.  The workspace: one sized by
+ * sv_chain_workspace_bytes (its header and per-request counters are used
+ * and left zeroed).
+ */
+sv_status sv_row_stats(const sv_chain_args* args, float* alpha, float* expected,
+                       void* workspace, size_t ws_bytes, sv_stream_t stream);
 
 /* Synchronise `stream`, read and clear the workspace error word.
    *device_flags receives the SV_DERR_* bits (may be NULL).  Returns SV_OK,

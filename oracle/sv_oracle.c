@@ -424,8 +424,10 @@ int svo_verify_tree(int B, int N, int M, int V, int dtype, int max_depth, int mo
     if (nn < 1 || nn > N || !(T >= 0.0) || mode < 0 || mode > 2) st = SVO_EARG;
     else if (par[0] != -1) st = SVO_ETREE;
     if (st == SVO_OK) depth[0] = 0;
+    /* q_row is checked only where the walk reads it (sampled, not naive) */
+    const int use_q = T > 0.0 && mode != SVO_TREE_NAIVE;
     for (int n = 1; st == SVO_OK && n < nn; ++n) {
-      if (par[n] < 0 || par[n] >= n || qr[n] < 0 || qr[n] >= M) st = SVO_ETREE;
+      if (par[n] < 0 || par[n] >= n || (use_q && (qr[n] < 0 || qr[n] >= M))) st = SVO_ETREE;
       else if (tok[n] < 0 || tok[n] >= V) st = SVO_ETOKEN;
       else {
         depth[n] = depth[par[n]] + 1;

@@ -20,7 +20,9 @@ from ._binding import (  # noqa: F401
     SV_MAX_TREE_NODES, SV_MAX_V, SV_OK, SpecVerifyError, lib, sv_chain_workspace_bytes,
     sv_get_error, sv_selftest_wait_timeout, sv_status_string, sv_tree_workspace_bytes,
     sv_verify_chain, sv_verify_tree, sv_version, sv_workspace_init,
-    SV_NOALLOC_SCRATCH_BYTES, sv_noalloc_get_error, sv_verify_chain_noalloc)
+    SV_NOALLOC_SCRATCH_BYTES, sv_noalloc_get_error, sv_verify_chain_noalloc,
+    SV_TREE_MSS, SV_TREE_MSS_NOREPLACE, SV_TREE_NAIVE, TREE_MODES, SV_MIN_WORKSPACE_BYTES,
+    sv_tree_mask, sv_row_stats)
 from ._build import build_library  # noqa: F401
 
 _ws_lock = threading.Lock()
@@ -85,8 +87,10 @@ def verify_chain(target_logits, draft_logits, draft_tokens, temperature, uniform
 
 def verify_tree(target_logits, draft_logits, node_tokens, parent, q_row, temperature,
                 u_accept, u_sample, max_depth: int, num_nodes=None,
-                ws: torch.Tensor | None = None) -> dict:
-    """Token-tree verification (MSS / VerifyGreedy) on the current stream.
+                ws: torch.Tensor | None = None, mode: str = "mss") -> dict:
+    """Token-tree verification on the current stream: VerifyGreedy for
+    temperature 0, otherwise the stochastic rule `mode` ("mss", "noreplace"
+    for children drawn without replacement, or "naive" sampling).
     Returns out_tokens [B][max_depth+1], out_len, accept_len and
     accepted_nodes [B][max_depth] (device tensors)."""
     B, N, V = target_logits.shape
@@ -104,9 +108,44 @@ def verify_tree(target_logits, draft_logits, node_tokens, parent, q_row, tempera
         ws = workspace(need, dev, "tree")
     sv_verify_tree(target_logits, draft_logits, node_tokens, parent, q_row, temperature,
                    u_accept, u_sample, out["out_tokens"], out["out_len"], out["accept_len"],
-                   out["accepted_nodes"], ws, max_depth=max_depth, num_nodes=num_nodes)
+                   out["accepted_nodes"], ws, max_depth=max_depth, num_nodes=num_nodes,
+                   mode=TREE_MODES[mode])
     if max_depth == 0:
         out["accepted_nodes"] = out["accepted_nodes"][:, :0]
+    return out
+
+
+def tree_mask(parent, num_nodes=None, words: int | None = None,
+              ws: torch.Tensor | None = None) -> dict:
+    """Tree-attention mask and depth position ids of DFS-linearised trees
+    (parent [B][N] int32 on the device).  Returns mask [B][N][words] (the
+    uint32 words in int32 storage: bit j of row i set iff j is i or an
+    ancestor of i) and depth [B][N] (device tensors)."""
+    B, N = parent.shape
+    W = (N + 31) // 32 if words is None else words
+    dev = parent.device
+    out = dict(mask=torch.empty((B, N, W), dtype=torch.int32, device=dev),
+               depth=torch.empty((B, N), dtype=torch.int32, device=dev))
+    if ws is None:
+        ws = workspace(SV_MIN_WORKSPACE_BYTES, dev, "mask")
+    sv_tree_mask(parent, out["mask"], out["depth"], ws, num_nodes=num_nodes)
+    return out
+
+
+def row_stats(target_logits, draft_logits, temperature, num_drafts=None, top_k=None,
+              ws: torch.Tensor | None = None) -> dict:
+    """Per-position acceptance rates alpha [B][K] (sum min(p_i, q_i)) and
+    the expected tokens per round [B] of a chain batch (device tensors)."""
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    dev = target_logits.device
+    out = dict(alpha=torch.empty((B, K), dtype=torch.float32, device=dev),
+               expected=torch.empty(B, dtype=torch.float32, device=dev))
+    if ws is None:
+        ws = workspace(sv_chain_workspace_bytes(max(B, 1), K, V, dtype_code(target_logits)),
+                       dev, "chain")
+    sv_row_stats(target_logits, draft_logits, temperature, out["alpha"], out["expected"], ws,
+                 num_drafts=num_drafts, top_k=top_k)
     return out
 
 

@@ -16,7 +16,8 @@ from ._build import LIBRARY
 
 SV_OK, SV_EINVAL, SV_ECUDA, SV_ETIMEOUT, SV_EDATA, SV_EWORKSPACE, SV_EUNSUPPORTED = range(7)
 SV_BF16, SV_FP32 = 0, 1
-SV_TREE_MSS = 0
+SV_TREE_MSS, SV_TREE_MSS_NOREPLACE, SV_TREE_NAIVE = 0, 1, 2
+TREE_MODES = {"mss": SV_TREE_MSS, "noreplace": SV_TREE_MSS_NOREPLACE, "naive": SV_TREE_NAIVE}
 SV_DERR_TOKEN, SV_DERR_NONFINITE, SV_DERR_MASS = 0x01, 0x02, 0x04
 SV_DERR_TREE, SV_DERR_TIMEOUT, SV_DERR_ARG = 0x08, 0x10, 0x20
 SV_MAX_K, SV_MAX_B, SV_MAX_V, SV_MAX_TOPK = 32, 1024, 1 << 20, 64
@@ -25,8 +26,9 @@ SV_MAX_TREE_NODES, SV_MAX_TREE_B = 64, 1024
 # every symbol include/specverify.h declares
 EXPORTS = ("sv_chain_workspace_bytes", "sv_tree_workspace_bytes", "sv_workspace_init",
            "sv_verify_chain", "sv_verify_tree", "sv_get_error", "sv_selftest_wait_timeout",
-           "sv_verify_chain_noalloc", "sv_noalloc_get_error",
+           "sv_verify_chain_noalloc", "sv_noalloc_get_error", "sv_tree_mask", "sv_row_stats",
            "sv_status_string", "sv_version")
+SV_MIN_WORKSPACE_BYTES = 8192
 SV_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 _P = ctypes.c_void_p
@@ -53,6 +55,11 @@ class SvTreeArgs(ctypes.Structure):
                 ("temperature", _P), ("top_k", _P), ("max_top_k", _i32),
                 ("u_accept", _P), ("u_sample", _P), ("out_tokens", _P), ("out_len", _P),
                 ("accept_len", _P), ("accepted_nodes", _P)]
+
+
+class SvTreeMaskArgs(ctypes.Structure):
+    _fields_ = [("B", _i32), ("N", _i32), ("words", _i32), ("parent", _P), ("num_nodes", _P),
+                ("mask", _P), ("depth", _P)]
 
 
 class SpecVerifyError(RuntimeError):
@@ -98,6 +105,10 @@ def lib(path: str | None = None):
     h.sv_verify_chain_noalloc.restype = ctypes.c_int
     h.sv_noalloc_get_error.argtypes = [_P, ctypes.POINTER(_i32)]
     h.sv_noalloc_get_error.restype = ctypes.c_int
+    h.sv_tree_mask.argtypes = [ctypes.POINTER(SvTreeMaskArgs), _P, ctypes.c_size_t, _P]
+    h.sv_tree_mask.restype = ctypes.c_int
+    h.sv_row_stats.argtypes = [ctypes.POINTER(SvChainArgs), _P, _P, _P, ctypes.c_size_t, _P]
+    h.sv_row_stats.restype = ctypes.c_int
     h.sv_status_string.argtypes = [ctypes.c_int]
     h.sv_status_string.restype = ctypes.c_char_p
     h.sv_version.argtypes = []
@@ -222,14 +233,14 @@ def sv_verify_chain(target_logits, draft_logits, draft_tokens, temperature, unif
 def sv_verify_tree(target_logits, draft_logits, node_tokens, parent, q_row, temperature,
                    u_accept, u_sample, out_tokens, out_len, accept_len, accepted_nodes,
                    workspace, max_depth: int, num_nodes=None, top_k=None, max_top_k: int = 0,
-                   stream=None) -> None:
+                   mode: int = SV_TREE_MSS, stream=None) -> None:
     """Enqueue sv_verify_tree on the current (or given) stream."""
     B, N, V = target_logits.shape
     a = SvTreeArgs()
     a.B, a.N, a.V, a.max_depth = B, N, V, max_depth
     a.M = draft_logits.shape[1] if draft_logits is not None else 1
     a.dtype = _dtype_code(target_logits)
-    a.mode = SV_TREE_MSS
+    a.mode = mode
     a.target_logits = _ptr(target_logits)
     a.target_row_stride = _row_stride(target_logits, N)
     if draft_logits is not None:
@@ -334,3 +345,54 @@ def sv_noalloc_get_error(stream=None) -> tuple[int, int]:
     flags = _i32(0)
     st = lib().sv_noalloc_get_error(_stream(stream), ctypes.byref(flags))
     return st, flags.value
+
+
+# ------------------------------------------------- tree mask, row statistics
+
+def sv_tree_mask(parent, mask, depth, workspace, num_nodes=None, stream=None) -> None:
+    """Enqueue sv_tree_mask: ancestor bitmask rows mask [B][N][words] (int32
+    storage of the uint32 words) and depths [B][N] of DFS-linearised trees."""
+    B, N = parent.shape
+    if mask.dim() != 3 or tuple(mask.shape[:2]) != (B, N):
+        raise ValueError("mask: expected [B][N][words]")
+    _check(parent, torch.int32, (B, N), "parent")
+    _check(num_nodes, torch.int32, (B,), "num_nodes")
+    _check(mask, torch.int32, (B, N, mask.shape[2]), "mask")
+    _check(depth, torch.int32, (B, N), "depth")
+    a = SvTreeMaskArgs()
+    a.B, a.N, a.words = B, N, mask.shape[2]
+    a.parent, a.num_nodes = _ptr(parent), _ptr(num_nodes)
+    a.mask, a.depth = _ptr(mask), _ptr(depth)
+    st = lib().sv_tree_mask(ctypes.byref(a), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream(stream))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "sv_tree_mask")
+
+
+def sv_row_stats(target_logits, draft_logits, temperature, alpha, expected, workspace,
+                 num_drafts=None, top_k=None, stream=None) -> None:
+    """Enqueue sv_row_stats: alpha [B][K] = sum min(p_i, q_i) per position
+    and expected [B] tokens per round."""
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    a = SvChainArgs()
+    a.B, a.K, a.V = B, K, V
+    a.dtype = _dtype_code(target_logits)
+    a.target_logits = _ptr(target_logits)
+    a.target_row_stride = _row_stride(target_logits, K1)
+    if K > 0:
+        if draft_logits is None or draft_logits.dtype != target_logits.dtype \
+                or tuple(draft_logits.shape) != (B, K, V):
+            raise ValueError("draft_logits must be [B][K][V] of the target's dtype")
+        a.draft_logits = _ptr(draft_logits)
+        a.draft_row_stride = _row_stride(draft_logits, K)
+    _check(temperature, torch.float32, (B,), "temperature")
+    _check(num_drafts, torch.int32, (B,), "num_drafts")
+    _check(top_k, torch.int32, (B,), "top_k")
+    _check(alpha, torch.float32, (B, K), "alpha")
+    _check(expected, torch.float32, (B,), "expected")
+    a.temperature, a.num_drafts, a.top_k = _ptr(temperature), _ptr(num_drafts), _ptr(top_k)
+    st = lib().sv_row_stats(ctypes.byref(a), _ptr(alpha), _ptr(expected), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream(stream))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "sv_row_stats")

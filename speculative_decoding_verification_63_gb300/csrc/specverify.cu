@@ -7,8 +7,10 @@
 
 #include "specverify.h"
 #include "sv_chain.cuh"
+#include "sv_stats.cuh"
 #include "sv_topk.cuh"
 #include "sv_tree.cuh"
+#include "sv_treemask.cuh"
 
 namespace {
 
@@ -401,7 +403,8 @@ sv_status sv_verify_tree(const sv_tree_args* a, void* workspace, size_t ws_bytes
   if (a->B < 0 || a->B > SV_MAX_TREE_B || a->N < 1 || a->N > SV_MAX_TREE_NODES || a->M < 1 ||
       a->M > SV_MAX_TREE_NODES || a->V < 1 || a->V > SV_MAX_V || a->max_depth < 0 ||
       a->max_depth >= a->N || (a->dtype != SV_BF16 && a->dtype != SV_FP32) ||
-      a->mode != SV_TREE_MSS || a->max_top_k < 0 || a->max_top_k > SV_MAX_TOPK)
+      a->mode < SV_TREE_MSS || a->mode > SV_TREE_NAIVE || a->max_top_k < 0 ||
+      a->max_top_k > SV_MAX_TOPK)
     return SV_EINVAL;
   if (a->B == 0) return SV_OK;
   if (a->target_logits == nullptr || a->target_row_stride < a->V || a->node_tokens == nullptr ||
@@ -432,6 +435,7 @@ sv_status sv_verify_tree(const sv_tree_args* a, void* workspace, size_t ws_bytes
   p.ipr = ipr;
   p.chunk_el = chunk_el;
   p.max_topk = a->max_top_k;
+  p.mode = static_cast<int>(a->mode);
   p.target = static_cast<const char*>(a->target_logits);
   p.t_stride = a->target_row_stride * es;
   p.draft = static_cast<const char*>(a->draft_logits);
@@ -489,6 +493,79 @@ sv_status sv_selftest_wait_timeout(void* workspace, size_t ws_bytes, int64_t lim
   return sv_get_error(workspace, stream, nullptr);
 }
 
+
+sv_status sv_tree_mask(const sv_tree_mask_args* a, void* workspace, size_t ws_bytes,
+                       sv_stream_t stream) {
+  if (a == nullptr) return SV_EINVAL;
+  if (a->B < 0 || a->B > SV_MAX_TREE_B || a->N < 1 || a->N > SV_MAX_TREE_NODES ||
+      a->words < (a->N + 31) / 32 || a->words > 1 << 20)
+    return SV_EINVAL;
+  if (a->B == 0) return SV_OK;
+  if (a->parent == nullptr || a->mask == nullptr || a->depth == nullptr) return SV_EINVAL;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0 ||
+      ws_bytes < SV_MIN_WORKSPACE_BYTES)
+    return SV_EWORKSPACE;
+  DeviceInfo dev;
+  const sv_status ds = device_info(dev);
+  if (ds != SV_OK) return ds;
+  MaskProblem p;
+  p.B = a->B;
+  p.N = a->N;
+  p.words = a->words;
+  p.parent = a->parent;
+  p.num_nodes = a->num_nodes;
+  p.mask = a->mask;
+  p.depth = a->depth;
+  p.hdr = static_cast<WsHeader*>(workspace);
+  tree_mask_kernel<<<(a->B + kMaskWarps - 1) / kMaskWarps, kMaskWarps * 32, 0,
+                     reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
+}
+
+sv_status sv_row_stats(const sv_chain_args* a, float* alpha, float* expected, void* workspace,
+                       size_t ws_bytes, sv_stream_t stream) {
+  if (a == nullptr) return SV_EINVAL;
+  if (a->B < 0 || a->B > SV_MAX_B || a->K < 0 || a->K > SV_MAX_K || a->V < 1 ||
+      a->V > SV_MAX_V || (a->dtype != SV_BF16 && a->dtype != SV_FP32))
+    return SV_EINVAL;
+  if (a->B == 0) return SV_OK;
+  if (a->target_logits == nullptr || a->target_row_stride < a->V || a->temperature == nullptr ||
+      expected == nullptr)
+    return SV_EINVAL;
+  if (a->K > 0 && (a->draft_logits == nullptr || a->draft_row_stride < a->V || alpha == nullptr))
+    return SV_EINVAL;
+  const Layout L = layout_for(0, 0, 0);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0 ||
+      ws_bytes < L.draws)
+    return SV_EWORKSPACE;
+  DeviceInfo dev;
+  const sv_status ds = device_info(dev);
+  if (ds != SV_OK) return ds;
+  const int es = es_of(a->dtype);
+  StatsProblem p;
+  p.B = a->B;
+  p.K = a->K;
+  p.V = a->V;
+  p.target = static_cast<const char*>(a->target_logits);
+  p.t_stride = a->target_row_stride * es;
+  p.draft = a->K > 0 ? static_cast<const char*>(a->draft_logits) : p.target;
+  p.d_stride = a->K > 0 ? a->draft_row_stride * es : p.t_stride;
+  p.vec = bulk_ok(p.target, p.t_stride, static_cast<int64_t>(a->V) * es) &&
+          bulk_ok(p.draft, p.d_stride, static_cast<int64_t>(a->V) * es);
+  p.num_drafts = a->num_drafts;
+  p.temperature = a->temperature;
+  p.top_k = a->top_k;
+  p.alpha = alpha;
+  p.expected = expected;
+  p.hdr = static_cast<WsHeader*>(workspace);
+  p.tickets = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + L.tickets);
+  const unsigned grid = static_cast<unsigned>(a->B) * static_cast<unsigned>(std::max(a->K, 1)) *
+                        static_cast<unsigned>(kStCluster);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (es == 2) row_stats_kernel<2><<<grid, kStThreads, 0, s>>>(p);
+  else row_stats_kernel<4><<<grid, kStThreads, 0, s>>>(p);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
+}
 
 sv_status sv_verify_chain_noalloc(const sv_chain_args* a, sv_stream_t stream) {
   if (a == nullptr) return SV_EINVAL;

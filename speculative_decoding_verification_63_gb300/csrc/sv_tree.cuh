@@ -10,11 +10,27 @@
 // r <- norm(max(0, r - q_c)); all rejected -> draw from r; a leaf -> draw
 // from p_node.  The residual lives in a per-request fp32 row of the
 // workspace (unnormalised, with its fp64 total).
+//
+// Two more stochastic rules (greedy walks do not depend on them):
+//   without replacement (children drawn without replacement; sec. 4.5 on
+//     the proof's precondition, sec. 10 exercise 7): the j-th child tried
+//     at a node is tested, and the residual formed, with q_j = q with the
+//     tokens of the siblings tried before it removed and renormalised:
+//     q_j(x) = q(x) / (1 - R) off the removed set (R = their q mass), 0 on
+//     it.  The residual pass uses the scaled q everywhere and then puts
+//     back r(y) at the removed tokens y.
+//   naive sampling (sec. 4.5): draw x from p_node with u_accept[node]; move
+//     to the first child whose token is x, else emit x.  No draft row is
+//     read.
 #pragma once
 
 #include "sv_kernel.cuh"
 
 namespace sv {
+
+constexpr int kTreeMss = 0;
+constexpr int kTreeNoReplace = 1;
+constexpr int kTreeNaive = 2;
 
 struct TreeProblem {
   static constexpr int kAuxBytes = 8;
@@ -23,6 +39,7 @@ struct TreeProblem {
   static constexpr bool kHasDirectFin = false;
   static constexpr bool kCtrl = false;
   int n_req, N, M, V, max_depth, es, ipr, chunk_el, max_topk;
+  int mode;          // kTreeMss, kTreeNoReplace or kTreeNaive
   bool bulk;
   const char* target;
   int64_t t_stride;
@@ -49,13 +66,15 @@ struct TreeProblem {
     const bool filtered = tk > 0 && tk < V;
     if (nn < 1 || nn > N || !(t >= 0.f) || tk < 0) return -1;
     if (t == 0.f) return KIND_ARGMAX;
-    if ((draft == nullptr && nn > 1) || filtered) return -1;  // top-k trees: not supported
+    if ((draft == nullptr && nn > 1 && mode != kTreeNaive) || filtered)
+      return -1;  // top-k trees: not supported
     return KIND_SOFTMAX;
   }
 
   // draft rows referenced by nodes 1..nn-1 (bit m = draft row m)
   __device__ unsigned long long ref_mask(int b, int nn) const {
     unsigned long long m = 0ull;
+    if (mode == kTreeNaive) return m;  // naive sampling reads no draft row
     for (int c = 1; c < nn; ++c) {
       const int r = q_row[static_cast<size_t>(b) * N + c];
       if (r >= 0 && r < M) m |= 1ull << r;
@@ -260,7 +279,7 @@ __device__ void TreeProblem::finalize(Shared& sh, const PosTables& tab, int pos,
         continue;
       }
       if (tok[cc] < 0 || tok[cc] >= V) err |= 0x01;
-      if (!greedy && (qr[cc] < 0 || qr[cc] >= M)) err |= 0x08;
+      if (!greedy && mode != kTreeNaive && (qr[cc] < 0 || qr[cc] >= M)) err |= 0x08;
       int d = 0, x = cc;
       while (x > 0 && d <= max_depth) {
         const int px = par[x];
@@ -287,6 +306,7 @@ __device__ void TreeProblem::finalize(Shared& sh, const PosTables& tab, int pos,
   __shared__ double s_w;
   __shared__ int w_mode;  // 0: r = p_node, 1: r = stored residual row w_cur / s_w
   __shared__ int w_cur;   // which of the two residual rows holds r
+  __shared__ double q_scale;  // 1 / (1 - removed q mass) (without replacement)
   while (!err) {
     // children of `node` in ascending index order
     if (warp == 0) {
@@ -327,6 +347,38 @@ __device__ void TreeProblem::finalize(Shared& sh, const PosTables& tab, int pos,
     }
     const char* prow = target + (static_cast<int64_t>(b) * N + node) * t_stride;
     const float mp = fs.rm[node], zp = fs.rz[node];
+    if (mode == kTreeNaive) {
+      // naive sampling: a draw from p_node with the node's own uniform
+      TreeWeights wp;
+      wp.prow = prow;
+      wp.wrow = nullptr;
+      wp.mp = mp;
+      wp.c = c;
+      wp.es = es;
+      wp.V = V;
+      wp.vec_ok = bulk;
+      const int x = icdf_draw(V, static_cast<double>(u_accept[static_cast<size_t>(b) * N + node]),
+                              wp, fs, ftid);
+      if (x < 0) {
+        err |= 0x04;
+        break;
+      }
+      int next = -1;
+      for (int k = 0; k < nc; ++k)
+        if (tok[children[k]] == x) {
+          next = children[k];
+          break;
+        }
+      if (next < 0) {
+        token = x;
+        break;
+      }
+      if (ftid == 0) path[L] = next;
+      ++L;
+      node = next;
+      named_sync(1, kFinThreads);
+      continue;
+    }
     int next = -1;
     for (int k = 0; k < nc; ++k) {
       const int ch = children[k];
@@ -337,10 +389,29 @@ __device__ void TreeProblem::finalize(Shared& sh, const PosTables& tab, int pos,
       const float* wsrc = ws.scratch + (static_cast<size_t>(b) * 2 + w_cur) * V;
       float* wdst = ws.scratch + (static_cast<size_t>(b) * 2 + (w_cur ^ 1)) * V;
       if (ftid == 0) {
+        // without replacement: q_j = q off the earlier siblings' tokens,
+        // scaled by 1 / (1 - R), R = their (distinct) q mass
+        double qs = 1.0;
+        bool removed = false;
+        if (mode == kTreeNoReplace && k > 0) {
+          double R = 0.0;
+          for (int j = 0; j < k; ++j) {
+            const int y = tok[children[j]];
+            bool dup = false;
+            for (int i = 0; i < j; ++i) dup |= tok[children[i]] == y;
+            if (dup) continue;
+            removed |= y == tok[ch];
+            R += exp2(static_cast<double>(load_logit(qrow, es, y) - mq) * cd) /
+                 static_cast<double>(zq);
+          }
+          qs = R < 1.0 ? 1.0 / (1.0 - R) : 0.0;
+        }
+        q_scale = qs;
         // accept test of child ch against the current residual r
         const int x = tok[ch];
-        const double q = exp2(static_cast<double>(load_logit(qrow, es, x) - mq) * cd) /
-                         static_cast<double>(zq);
+        const double q = removed ? 0.0
+                                 : exp2(static_cast<double>(load_logit(qrow, es, x) - mq) * cd) /
+                                       static_cast<double>(zq) * qs;
         const double r =
             w_mode == 0
                 ? exp2(static_cast<double>(load_logit(prow, es, x) - mp) * cd) /
@@ -357,12 +428,16 @@ __device__ void TreeProblem::finalize(Shared& sh, const PosTables& tab, int pos,
       // rejected: r <- max(0, r - q_ch) into the other residual row
       const float izq = 1.f / zq, izp = 1.f / zp;
       const float inv_sw = w_mode == 0 ? 0.f : static_cast<float>(1.0 / s_w);
-      const int mode = w_mode;
+      const float qsf = static_cast<float>(q_scale);
+      const int rmode = w_mode;
+      auto r_at = [&](int t) {
+        return rmode == 0 ? fast_exp2(scaled_arg(load_logit(prow, es, t), mp, c)) * izp
+                          : __ldcg(wsrc + t) * inv_sw;
+      };
       float part = 0.f;
       for (int t = ftid; t < V; t += kFinThreads) {
-        const float rt = mode == 0 ? fast_exp2(scaled_arg(load_logit(prow, es, t), mp, c)) * izp
-                                   : __ldcg(wsrc + t) * inv_sw;
-        const float qt = fast_exp2(scaled_arg(load_logit(qrow, es, t), mq, c)) * izq;
+        const float rt = r_at(t);
+        const float qt = fast_exp2(scaled_arg(load_logit(qrow, es, t), mq, c)) * izq * qsf;
         const float wt = fmaxf(rt - qt, 0.f);
         part += wt;
         __stcg(wdst + t, wt);
@@ -375,6 +450,18 @@ __device__ void TreeProblem::finalize(Shared& sh, const PosTables& tab, int pos,
       if (ftid == 0) {
         double S = 0.0;
         for (int w = 0; w < kFinWarps; ++w) S += fs.dsum[w];
+        if (mode == kTreeNoReplace) {
+          // q_j is 0 on the removed tokens: the residual there is r itself
+          for (int j = 0; j < k; ++j) {
+            const int y = tok[children[j]];
+            bool dup = false;
+            for (int i = 0; i < j; ++i) dup |= tok[children[i]] == y;
+            if (dup) continue;
+            const float ry = r_at(y);
+            S += static_cast<double>(ry) - static_cast<double>(__ldcg(wdst + y));
+            __stcg(wdst + y, ry);
+          }
+        }
         if (S > 0.0) {  // zero mass (rounding only) keeps r as it was
           s_w = S;
           w_mode = 1;

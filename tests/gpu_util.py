@@ -39,12 +39,14 @@ def run_chain(inp, with_probs=True, ws=None, num_drafts=True, top_k=True):
     return {k: v.cpu().numpy() for k, v in out.items()}
 
 
-def run_tree(inp, ws=None):
-    out = sv.verify_tree(dev(inp["target"]), dev(inp["draft"]), dev(inp["node_tokens"]),
+def run_tree(inp, ws=None, mode=None):
+    mode = mode or inp.get("mode", "mss")
+    out = sv.verify_tree(dev(inp["target"]), None if mode == "naive" else dev(inp["draft"]),
+                         dev(inp["node_tokens"]),
                          dev(inp["parent"]), dev(inp["q_row"]), dev(inp["temperature"]),
                          dev(inp["u_accept"]), dev(inp["u_sample"]),
                          max_depth=int(inp["max_depth"]), num_nodes=dev(inp["num_nodes"]),
-                         ws=ws)
+                         ws=ws, mode=mode)
     torch.cuda.synchronize()
     return {k: v.cpu().numpy() for k, v in out.items()}
 
@@ -116,6 +118,6 @@ def tree_path_tokens(inp, got):
 
 def check_tree(inp, **kw):
     got = run_tree(inp, **kw)
-    ref = oracle.verify_tree_inputs(inp)
+    ref = oracle.verify_tree_inputs(inp, mode=kw.get("mode"))
     return compare(got, ref, inp["N"], prefix_tokens=tree_path_tokens(inp, got),
                    V=inp["V"]), got, ref

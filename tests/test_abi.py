@@ -46,7 +46,8 @@ def test_struct_layout_matches_binding(tmp_path):
              "int main(void) {"]
     expect = []
     for cname, cls in [("sv_chain_args", _binding.SvChainArgs),
-                       ("sv_tree_args", _binding.SvTreeArgs)]:
+                       ("sv_tree_args", _binding.SvTreeArgs),
+                       ("sv_tree_mask_args", _binding.SvTreeMaskArgs)]:
         lines.append(f'printf("%zu\\n", sizeof({cname}));')
         expect.append(ctypes.sizeof(cls))
         for f, _ in cls._fields_:
@@ -116,6 +117,39 @@ def test_host_side_checks(svlib):
     t = b.SvTreeArgs()
     t.B, t.N, t.M, t.V, t.max_depth = 2, 8, 8, 100, 8  # max_depth must be < N
     assert svlib.sv_verify_tree(ctypes.byref(t), ws_ok, big, None) == b.SV_EINVAL
+    t.max_depth = 3
+    t.mode = 3  # no such tree mode
+    assert svlib.sv_verify_tree(ctypes.byref(t), ws_ok, big, None) == b.SV_EINVAL
+    # tree mask
+    m = b.SvTreeMaskArgs()
+    m.B, m.N, m.words = 4, 40, 2
+    m.parent = m.mask = m.depth = 0x100000
+    mcall = lambda a, ws=ws_ok, n=big: svlib.sv_tree_mask(ctypes.byref(a), ws, n, None)
+    assert svlib.sv_tree_mask(None, ws_ok, big, None) == b.SV_EINVAL
+    m0 = b.SvTreeMaskArgs()
+    m0.B, m0.N, m0.words = 0, 8, 1
+    assert mcall(m0) == b.SV_OK
+    m.words = 1  # 40 nodes need two words
+    assert mcall(m) == b.SV_EINVAL
+    m.words, m.N = 2, b.SV_MAX_TREE_NODES + 1
+    assert mcall(m) == b.SV_EINVAL
+    m.N, m.parent = 40, None
+    assert mcall(m) == b.SV_EINVAL
+    m.parent = 0x100000
+    assert mcall(m, n=b.SV_MIN_WORKSPACE_BYTES - 1) == b.SV_EWORKSPACE
+    assert mcall(m, ws=ctypes.c_void_p(0x200010)) == b.SV_EWORKSPACE
+    # row statistics
+    al, ex = ctypes.c_void_p(0x300000), ctypes.c_void_p(0x400000)
+    scall = lambda a, al=al, ex=ex, ws=ws_ok, n=big: svlib.sv_row_stats(ctypes.byref(a), al, ex,
+                                                                        ws, n, None)
+    assert svlib.sv_row_stats(None, al, ex, ws_ok, big, None) == b.SV_EINVAL
+    assert scall(_chain_args(b, B=0)) == b.SV_OK
+    assert scall(_chain_args(b, K=b.SV_MAX_K + 1)) == b.SV_EINVAL
+    assert scall(_chain_args(b), ex=None) == b.SV_EINVAL
+    assert scall(_chain_args(b), al=None) == b.SV_EINVAL
+    assert scall(_chain_args(b, draft_logits=None)) == b.SV_EINVAL
+    assert scall(_chain_args(b, temperature=None)) == b.SV_EINVAL
+    assert scall(_chain_args(b), n=1024) == b.SV_EWORKSPACE
     assert svlib.sv_get_error(None, None, None) == b.SV_EWORKSPACE
     assert svlib.sv_selftest_wait_timeout(None, 0, 1000, None) == b.SV_EWORKSPACE
     assert svlib.sv_workspace_init(None, 0, None) == b.SV_EWORKSPACE
