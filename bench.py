@@ -106,14 +106,19 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# the sources the chain verification kernel is compiled from
+CHAIN_KERNEL_SOURCES = ("sv_device.cuh", "sv_rowpass.cuh", "sv_kernel.cuh", "sv_chain.cuh",
+                        "sv_topk.cuh")
+
+
 def source_hash() -> str:
-    """Hash of the CUDA sources, to tell whether a stored ncu figure is current."""
+    """Hash of the chain kernel's CUDA sources, to tell whether a stored ncu
+    figure is current."""
     d = os.path.join(ROOT, "speculative_decoding_verification_63_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(d)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(d, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in CHAIN_KERNEL_SOURCES:
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
