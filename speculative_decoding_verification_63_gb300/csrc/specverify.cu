@@ -20,7 +20,7 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 struct Layout {
-  size_t tickets, draws, jobs, topk_done, partials, segsums, scratch, total;
+  size_t tickets, jobs, topk_done, partials, segsums, scratch, total;
 };
 
 // top-k pass: one counter per row (b, i) of a chain call
@@ -32,7 +32,7 @@ static_assert(2 * SV_MAX_K + 1 <= 96, "top-k finalize: row statistics in three l
 static_assert(SV_MAX_V / kRSeg <= kMaxPages * kPageSeg && 2 * kMaxPages <= kMaxRowsPerReq,
               "draw finalize pages");
 
-// The header, the tickets (requests, then their draws), the draw list and
+// The header, the tickets (requests, then their draws), the draw records and
 // the top-k pass's row counters sit at fixed offsets with a fixed capacity
 // (SV_MAX_B requests), so the region that every call leaves zeroed is the
 // same for all problem sizes: one initialised workspace serves chain and
@@ -40,9 +40,9 @@ static_assert(SV_MAX_V / kRSeg <= kMaxPages * kPageSeg && 2 * kMaxPages <= kMaxR
 Layout layout_for(int64_t partial_slots, int64_t segsum_floats, int64_t scratch_floats) {
   Layout L;
   L.tickets = align_up(sizeof(WsHeader));
-  L.draws = align_up(L.tickets + sizeof(unsigned int) * 2 * static_cast<size_t>(SV_MAX_B));
-  L.jobs = align_up(L.draws + sizeof(int) * static_cast<size_t>(SV_MAX_B));
-  L.topk_done = align_up(L.jobs + sizeof(P2Job) * static_cast<size_t>(SV_MAX_B));
+  L.jobs = align_up(L.tickets + sizeof(unsigned int) * 2 * static_cast<size_t>(SV_MAX_B));
+  L.topk_done = align_up(L.jobs + sizeof(unsigned long long) * kJobWords *
+                                      static_cast<size_t>(SV_MAX_B));
   L.partials = align_up(L.topk_done + sizeof(unsigned int) * kTopkRows);
   L.segsums = align_up(L.partials + sizeof(float2) * static_cast<size_t>(partial_slots));
   L.scratch = align_up(L.segsums + sizeof(float) * static_cast<size_t>(segsum_floats));
@@ -55,7 +55,6 @@ Ws ws_view(void* base, const Layout& L) {
   Ws w;
   w.hdr = reinterpret_cast<WsHeader*>(p);
   w.tickets = reinterpret_cast<unsigned int*>(p + L.tickets);
-  w.draws = reinterpret_cast<int*>(p + L.draws);
   w.partials = reinterpret_cast<float2*>(p + L.partials);
   w.segsums = reinterpret_cast<float*>(p + L.segsums);
   w.jobs = reinterpret_cast<void*>(p + L.jobs);
@@ -347,7 +346,7 @@ sv_status sv_verify_chain(const sv_chain_args* a, void* workspace, size_t ws_byt
   p.p_at = a->p_at_draft;
   p.q_at = a->q_at_draft;
   p.ws = ws_view(workspace, L);
-  p.jobs = static_cast<P2Job*>(p.ws.jobs);
+  p.jobs = static_cast<unsigned long long*>(p.ws.jobs);
   p.chunk2 = resid_chunk_el_of(a->dtype);
   p.ipr2 = (a->V + p.chunk2 - 1) / p.chunk2;
   char* scratch = reinterpret_cast<char*>(p.ws.scratch);
@@ -536,7 +535,7 @@ sv_status sv_row_stats(const sv_chain_args* a, float* alpha, float* expected, vo
     return SV_EINVAL;
   const Layout L = layout_for(0, 0, 0);
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0 ||
-      ws_bytes < L.draws)
+      ws_bytes < L.jobs)
     return SV_EWORKSPACE;
   DeviceInfo dev;
   const sv_status ds = device_info(dev);

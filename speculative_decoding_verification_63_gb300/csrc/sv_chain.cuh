@@ -54,7 +54,7 @@ struct ChainProblem {
   int* accept_len;
   float* p_at;
   float* q_at;
-  P2Job* jobs;  // [SV_MAX_B] the draw of request b
+  unsigned long long* jobs;  // [SV_MAX_B][kJobWords] the draw of request b (see P2Job)
   const float2* topk_lists;  // [B (2K+1)][max_topk] top-k (logit, id) of row (b, i), token order
   const float2* topk_mz;     // [B (2K+1)] (m, Z) over those logits
   Ws ws;
@@ -153,18 +153,69 @@ struct ChainProblem {
     rm.fin_code = mt.pos;
   }
 
-  __device__ P2Job load_job(int b) const {
+  // Publish request b's draw (or its failure) as three self-marking words.
+  __device__ void publish_job(int b, const P2Job* jb) const {
+    unsigned long long* w = jobs + static_cast<size_t>(b) * kJobWords;
+    if (jb) {
+      st_relaxed_u64(w, __float_as_uint(jb->izp) |
+                            static_cast<unsigned long long>(__float_as_uint(jb->mp)) << 32);
+      const unsigned lo = jb->mode == 0 ? __float_as_uint(jb->izq) : 0x80000000u;
+      st_relaxed_u64(w + 1, lo | static_cast<unsigned long long>(__float_as_uint(jb->mq)) << 32);
+      st_relaxed_u64(w + 2, static_cast<unsigned long long>(1 + jb->n + (jb->mode << 8)));
+    } else {
+      st_relaxed_u64(w, 0x80000000ull);
+      st_relaxed_u64(w + 1, 0x80000000ull);
+      st_relaxed_u64(w + 2, 1ull | 1ull << 32);
+    }
+  }
+  // Decode the words of request b's draw (all nonzero); false if it failed.
+  __device__ bool decode_job(int b, const unsigned long long (&w)[3], Scale2 c, P2Job& j) const {
+    const unsigned meta = static_cast<unsigned>(w[2]);
+    j.b = b;
+    j.n = static_cast<int>(meta & 0xffu) - 1;
+    j.mode = static_cast<int>(meta >> 8);
+    j.izp = __uint_as_float(static_cast<unsigned>(w[0]));
+    j.mp = __uint_as_float(static_cast<unsigned>(w[0] >> 32));
+    j.izq = j.mode == 0 ? __uint_as_float(static_cast<unsigned>(w[1])) : 0.f;
+    j.mq = __uint_as_float(static_cast<unsigned>(w[1] >> 32));
+    j.c_hi = c.hi;
+    j.c_lo = c.lo;
+    return (w[2] >> 32) == 0ull;
+  }
+  // The draw at position d of the processing order (sampled requests hold
+  // positions 0 .. number of sampled requests - 1), polled until published:
+  // returns 1 (a draw), 0 (the request failed: no draw) or -1 (the wait
+  // expired).
+  __device__ int poll_job(const PosTables& tab, int d, uint64_t limit, P2Job& j) const {
+    const int b = info_req(tab.info[d]);
+    const unsigned long long* p = jobs + static_cast<size_t>(b) * kJobWords;
+    unsigned long long w[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) w[k] = ld_relaxed_u64(p + k);
+    const uint64_t t0 = globaltimer_ns();
+    unsigned backoff = 32;
+    while (w[0] == 0ull || w[1] == 0ull || w[2] == 0ull) {
+      if (globaltimer_ns() - t0 > limit) return -1;
+      __nanosleep(backoff);
+      backoff = min(backoff * 2u, 128u);
+#pragma unroll
+      for (int k = 0; k < 3; ++k)
+        if (w[k] == 0ull) w[k] = ld_relaxed_u64(p + k);
+    }
+    j.pos = d;
+    return decode_job(b, w, Scale2{tab.scale[d].x, tab.scale[d].y}, j) ? 1 : 0;
+  }
+  // The draw of the request at position pos, read back by the warp that
+  // published it.
+  __device__ P2Job load_job(const PosTables& tab, int pos) const {
+    const int b = info_req(tab.info[pos]);
+    const unsigned long long* p = jobs + static_cast<size_t>(b) * kJobWords;
+    unsigned long long w[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) w[k] = ld_relaxed_u64(p + k);
     P2Job j;
-    const P2Job* g = jobs + b;
-    j.b = __ldcg(&g->b);
-    j.n = __ldcg(&g->n);
-    j.mode = __ldcg(&g->mode);
-    j.mp = __ldcg(&g->mp);
-    j.izp = __ldcg(&g->izp);
-    j.mq = __ldcg(&g->mq);
-    j.izq = __ldcg(&g->izq);
-    j.c_hi = __ldcg(&g->c_hi);
-    j.c_lo = __ldcg(&g->c_lo);
+    j.pos = pos;
+    decode_job(b, w, Scale2{tab.scale[pos].x, tab.scale[pos].y}, j);
     return j;
   }
 
@@ -185,7 +236,7 @@ struct ChainProblem {
     rm.slot = (jb.b * ipr2 + chunk) * segs_per_chunk();
     rm.tkt = kDrawTicketBase + jb.b;
     rm.need = ipr2;
-    rm.fin_code = jb.b | kFinResid;
+    rm.fin_code = jb.pos | kFinResid;
   }
 
   // draw pass: warp w of the group reduces segments w * spw + s (s < spw)
@@ -305,29 +356,21 @@ struct ChainProblem {
                    (static_cast<unsigned long long>(hi) << 32) | __float_as_uint(v.x));
   }
   // A draw chunk's segment sums of consumer warp w (spw of them), stored
-  // where the draw finalize polls them (sums are >= 0; the finalize fills
-  // the slots with -1 before it publishes the draw).
+  // sign-flipped (enc_seg: never the zero word) where the draw finalize
+  // polls them; zero marks a sum not yet written.
   __device__ void store_segsums_warp(int base, int w, float4 v) const {
     const int spw = segs_per_chunk() / kGroupWarps;
-    float* d = ws.segsums + base + w * spw;
+    unsigned* d = reinterpret_cast<unsigned*>(ws.segsums) + base + w * spw;
     const float x[4] = {v.x, v.y, v.z, v.w};
-    for (int k = 0; k < spw; ++k)
-      asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(d + k), "f"(x[k]) : "memory");
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (k < spw)
+        asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(d + k), "r"(enc_seg(x[k]))
+                     : "memory");
   }
   __device__ void store_segsums(const ResMeta& rm, int lane, float4 v) const {
-    const int spw = segs_per_chunk() / kGroupWarps;
-    if (lane < kGroupWarps) {
-      float* d = ws.segsums + rm.slot + lane * spw;
-      if (spw == 4) {
-        *reinterpret_cast<float4*>(d) = v;
-      } else {
-        d[0] = v.x;
-        if (spw > 1) d[1] = v.y;
-        if (spw > 2) d[2] = v.z;
-      }
-    }
+    if (lane < kGroupWarps) store_segsums_warp(rm.slot, lane, v);
   }
-
   __device__ float4 consume(const StageMeta& mt, const unsigned char* sp, uint64_t* empty_bar,
                             int ctid, int lane) const {
     if (mt.kind == KIND_RESID_PASS) return consume_resid(mt, sp, empty_bar, ctid, lane);
@@ -341,157 +384,143 @@ struct ChainProblem {
   }
   __device__ void finalize_warp(Shared& sh, const PosTables& tab, int code, int lane,
                                 WarpFin& wf) const {
-    if (code & kFinResid) draw_finalize(code & ~kFinResid, lane, wf);
+    if (code & kFinResid) draw_finalize(sh, tab, code & ~kFinResid, lane, wf);
     else if (info_kind(tab.info[code]) == KIND_TOPK) topk_finalize(tab, code, lane, wf);
     else request_finalize(sh, tab, code, lane, wf);
   }
-  // Control CTAs: the finalize of position pos once every chunk of its rows
-  // is booked (returns 1 when it published a draw), and the draw finalize
-  // once every chunk of that draw is booked.  The waits poll the request's
-  // ticket with acquire loads and are bounded.
+  // Control CTAs: the finalize of position pos (returns 1 when it published
+  // a draw), and the draw finalize of a published draw.  Each polls the data
+  // words it needs -- the request's chunk partials, the draw's segment sums
+  // -- with bounded waits: every word is written once per call and is never
+  // zero once written, so no count or fence stands between the last chunk
+  // and its finalize.
   __device__ int ctrl_request(Shared& sh, const PosTables& tab, int pos, int lane,
                               WarpFin& wf) const {
     const int info = tab.info[pos];
-    const int b = info_req(info), kind = info_kind(info);
+    const int kind = info_kind(info);
     const int rows = tab.rstart[pos + 1] - tab.rstart[pos];
     if (kind == KIND_TOPK) {
       topk_finalize(tab, pos, lane, wf);
       return 0;
     }
     if (rows == 0) return 0;  // invalid arguments: failed in the preamble
-    // the request's chunk partials: rows rstart[pos] .. (lane j polls row j,
-    // the row it merges); zero marks a slot not yet written
+    const int drew = request_finalize(sh, tab, pos, lane, wf);
+    // leave the request's partial slots zero for the next call
     unsigned long long* w =
         reinterpret_cast<unsigned long long*>(ws.partials) + static_cast<size_t>(tab.rstart[pos]) * ipr;
-    // the progress count first (one word: cheap to poll), then the words
-    // themselves (the count is not ordered with them)
-    if (!wait_ticket(sh, ws.tickets + b, static_cast<unsigned>(rows * ipr), lane) ||
-        !wait_rows(sh, w, rows, ipr, lane)) {
-      if (lane == 0) write_failed(b, 0x10);
-      return 0;
-    }
-    const int drew = request_finalize(sh, tab, pos, lane, wf);
-    // leave the slots zero for the next call
     for (int j = lane; j < rows; j += 32)
       for (int c = 0; c < ipr; ++c) st_relaxed_u64(w + static_cast<size_t>(j) * ipr + c, 0ull);
     return drew;
   }
-  // Wait, bounded, until every word of rows 0..rows-1 (ipr words each) is
-  // nonzero: lane j polls row j (and j + 32, ...).
-  __device__ bool wait_rows(Shared& sh, const unsigned long long* w, int rows, int n,
-                            int lane) const {
-    const uint64_t t0 = globaltimer_ns();
-    unsigned backoff = 32;
-    int next = 0;  // first word of this lane's rows not yet seen written
-    const int mine = rows > lane ? ((rows - 1 - lane) / 32 + 1) * n : 0;
-    for (;;) {
-      while (next < mine) {
-        const int j = lane + 32 * (next / n), c = next % n;
-        if (ld_relaxed_u64(w + static_cast<size_t>(j) * n + c) == 0ull) break;
-        ++next;
-      }
-      if (__all_sync(0xffffffffu, next >= mine)) {
-        __syncwarp();
-        return true;
-      }
-      if (globaltimer_ns() - t0 > (sh.timed_out ? kWaitLimitAfterTimeoutNs : kWaitLimitNs)) {
-        sh.timed_out = 1;
-        return false;
-      }
-      __nanosleep(backoff);
-      backoff = min(backoff * 2u, 256u);
-    }
-  }
   __device__ void ctrl_draw(Shared& sh, const PosTables& tab, int pos, int lane,
                             WarpFin& wf) const {
-    const int b = info_req(tab.info[pos]);
-    // the draw's segment sums, polled in the layout the draw finalize reads
-    // them (lane l: 16 consecutive sums of each page of 512)
-    const int nseg = ipr2 * segs_per_chunk();
-    const float* ss = ws.segsums + static_cast<size_t>(b) * nseg;
-    if (!wait_ticket(sh, ws.tickets + kDrawTicketBase + b,
-                     static_cast<unsigned>(ipr2), lane)) {
-      if (lane == 0) write_failed(b, 0x10);
-      return;
-    }
-    const uint64_t t0 = globaltimer_ns();
-    unsigned backoff = 32;
-    int next = 0;
-    const int npages = (nseg + kPageSeg - 1) / kPageSeg;
-    for (;;) {
-      while (next < npages * 16) {
-        const int i = (next / 16) * kPageSeg + lane * 16 + next % 16;
-        if (i < nseg && !(ld_relaxed_f32(ss + i) >= 0.f)) break;
-        ++next;
-      }
-      if (__all_sync(0xffffffffu, next >= npages * 16)) break;
-      if (globaltimer_ns() - t0 > (sh.timed_out ? kWaitLimitAfterTimeoutNs : kWaitLimitNs)) {
-        sh.timed_out = 1;
-        if (lane == 0) write_failed(b, 0x10);
-        return;
-      }
-      __nanosleep(backoff);
-      backoff = min(backoff * 2u, 256u);
-    }
-    __syncwarp();
-    draw_finalize(b, lane, wf);
+    draw_finalize(sh, tab, pos, lane, wf);
   }
   __device__ void topk_finalize(const PosTables& tab, int pos, int lane, WarpFin& wf) const;
   __device__ int request_finalize(Shared& sh, const PosTables& tab, int pos, int lane,
                                    WarpFin& wf) const;
-  __device__ void draw_finalize(int b, int lane, WarpFin& wf) const;
-  __device__ void last_cta_reset() const {}
+  __device__ void draw_finalize(Shared& sh, const PosTables& tab, int pos, int lane,
+                                WarpFin& wf) const;
+  // A claim of the failed draw at position d (the record says failed): the
+  // ipr2 claims of the draw each count themselves in the record's spare
+  // word, and the last one clears the record for the next call -- every
+  // other claim has read it by then.
+  __device__ void failed_claim(const PosTables& tab, int d) const {
+    unsigned long long* w = jobs + static_cast<size_t>(info_req(tab.info[d])) * kJobWords;
+    if (atomicAdd(w + 3, 1ull) == static_cast<unsigned long long>(ipr2 - 1))
+      for (int k = 0; k < kJobWords; ++k) st_relaxed_u64(w + k, 0ull);
+  }
 };
 
-// Merge the chunk partials of a request's rows into wf: lane j takes row j
-// (passes of 32 rows) and reads its ipr partials itself, eight loads in
-// flight at a time -- no shuffles, and one exp2 per partial, because the
-// consumers keep the shared-memory and special-function pipes of the SM
-// busy while finalizes run.  Softmax rows: the maximum first, then each
-// sum rescaled once to it; argmax rows: the largest value, lowest index.
-__device__ __forceinline__ void merge_rows(const float2* partials, int r0, int nrows, int ipr,
-                                           bool greedy, Scale2 c, int lane, WarpFin& wf) {
-  for (int j = lane; j < nrows; j += 32) {
-    const float2* pp = partials + static_cast<size_t>(r0 + j) * ipr;
-    float2 t[8];
+// Eight consecutive chunk partials of a row (words c0 .. c0 + 7 below n;
+// `fill` for the rest), polled until every one is written: a written word
+// is never zero.  The back-off is short, and shorter once part of the batch
+// is in, since the rest of a row lands within a chunk time: the finalize
+// that follows is on the step's critical path.  False when the wait
+// expired.
+__device__ __forceinline__ bool poll_words8(const unsigned long long* w, int c0, int n,
+                                            unsigned long long fill, unsigned long long (&t)[8],
+                                            uint64_t t0, uint64_t limit) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) t[k] = c0 + k < n ? ld_relaxed_u64(w + c0 + k) : fill;
+  unsigned backoff = 64;
+  for (;;) {
+    int missing = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) missing += t[k] == 0ull;
+    if (missing == 0) return true;
+    if (globaltimer_ns() - t0 > limit) return false;
+    __nanosleep(backoff);
+    backoff = missing < 8 ? 32u : min(backoff * 2u, 256u);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (t[k] == 0ull) t[k] = ld_relaxed_u64(w + c0 + k);
+  }
+}
+
+__device__ __forceinline__ float2 word_f2(unsigned long long v) {
+  return make_float2(__uint_as_float(static_cast<unsigned>(v)),
+                     __uint_as_float(static_cast<unsigned>(v >> 32)));
+}
+
+// Merge the chunk partials of a request's rows into wf as they are
+// written: lane j takes row j (passes of 32 rows), polls its ipr partials
+// eight at a time and merges them from the polled values -- one exp2 per
+// partial, no shuffles, because the consumers keep the shared-memory and
+// special-function pipes of the SM busy while finalizes run.  Softmax rows:
+// the maximum first, then each sum rescaled once to it; argmax rows: the
+// largest value, lowest index (the partial's high word is index + 1).
+// False in every lane when a wait expired.
+__device__ __forceinline__ bool merge_rows(const float2* partials, int r0, int nrows, int ipr,
+                                           bool greedy, Scale2 c, int lane, WarpFin& wf,
+                                           uint64_t limit) {
+  const uint64_t t0 = globaltimer_ns();
+  bool ok = true;
+  for (int j = lane; j < nrows && ok; j += 32) {
+    const unsigned long long* pp =
+        reinterpret_cast<const unsigned long long*>(partials) + static_cast<size_t>(r0 + j) * ipr;
+    unsigned long long t[8];
     if (greedy) {
       VI v{kNegInf, 0x7fffffff};
-      for (int c0 = 0; c0 < ipr; c0 += 8) {
+      const unsigned long long fill =
+          (static_cast<unsigned long long>(0x7fffffffu) << 32) | __float_as_uint(kNegInf);
+      for (int c0 = 0; c0 < ipr && ok; c0 += 8) {
+        ok = poll_words8(pp, c0, ipr, fill, t, t0, limit);
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          t[k] = c0 + k < ipr ? __ldcg(pp + c0 + k)
-                              : make_float2(kNegInf, __int_as_float(0x7fffffff));
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (c0 + k < ipr) v = vi_better(v, VI{t[k].x, __float_as_int(t[k].y) - 1});
+        for (int k = 0; k < 8; ++k) {
+          const float2 f = word_f2(t[k]);
+          if (c0 + k < ipr) v = vi_better(v, VI{f.x, __float_as_int(f.y) - 1});
+        }
       }
       wf.rm[j] = v.v;
       wf.ridx[j] = v.i;
     } else {
+      const unsigned long long fill = __float_as_uint(kNegInf);
       float M = kNegInf;
       bool nan = false;
-      for (int c0 = 0; c0 < ipr; c0 += 8) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) t[k] = c0 + k < ipr ? __ldcg(pp + c0 + k) : make_float2(kNegInf, 0.f);
+      for (int c0 = 0; c0 < ipr && ok; c0 += 8) {
+        ok = poll_words8(pp, c0, ipr, fill, t, t0, limit);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          nan |= t[k].x != t[k].x;
-          M = fmaxf(M, t[k].x);
+          const float x = word_f2(t[k]).x;
+          nan |= x != x;
+          M = fmaxf(M, x);
         }
       }
       float sum = 0.f;
-      if (!nan && M != kNegInf) {
+      if (ok && !nan && M != kNegInf) {
         for (int c0 = 0; c0 < ipr; c0 += 8) {
-          // t holds the last batch of the maximum pass: reload unless that
-          // batch is the first (a row of at most eight chunks)
+          // t holds the last batch of the maximum pass: reload (every word
+          // is written by now) unless that batch is the first
           if (c0 > 0 || ipr > 8) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              t[k] = c0 + k < ipr ? __ldcg(pp + c0 + k) : make_float2(kNegInf, 0.f);
+            for (int k = 0; k < 8; ++k) t[k] = c0 + k < ipr ? ld_relaxed_u64(pp + c0 + k) : fill;
           }
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            if (t[k].x != kNegInf) sum += t[k].y * fast_exp2(scaled_arg(t[k].x, M, c));
+          for (int k = 0; k < 8; ++k) {
+            const float2 f = word_f2(t[k]);
+            if (f.x != kNegInf) sum += f.y * fast_exp2(scaled_arg(f.x, M, c));
+          }
         }
       }
       wf.rm[j] = nan ? nan_f() : M;
@@ -499,6 +528,7 @@ __device__ __forceinline__ void merge_rows(const float2* partials, int r0, int n
     }
   }
   __syncwarp();
+  return __all_sync(0xffffffffu, ok);
 }
 
 __device__ int ChainProblem::request_finalize(Shared& sh, const PosTables& tab, int pos,
@@ -510,8 +540,8 @@ __device__ int ChainProblem::request_finalize(Shared& sh, const PosTables& tab, 
   const Scale2 c{tab.scale[pos].x, tab.scale[pos].y};
   const bool greedy = kind == KIND_ARGMAX;
 
-  // loads that do not depend on the merge go out first: the draft tokens,
-  // their uniforms and the logits they gather
+  // loads that do not depend on the main pass go out before its partials
+  // are polled: the draft tokens, their uniforms and the logits they gather
   const int x = lane < nd ? tokens[static_cast<size_t>(b) * K + lane] : 0;
   const float ui = lane < nd ? uniforms[static_cast<size_t>(b) * (K + 1) + lane] : 0.f;
   const bool x_ok = x >= 0 && x < V;
@@ -520,7 +550,16 @@ __device__ int ChainProblem::request_finalize(Shared& sh, const PosTables& tab, 
     lx = load_logit(trow(b, lane), es, x);
     dx = load_logit(drow(b, lane), es, x);
   }
-  merge_rows(ws.partials, r0, nrows, ipr, greedy, c, lane, wf);
+  if (!merge_rows(ws.partials, r0, nrows, ipr, greedy, c, lane, wf,
+                  sh.timed_out ? kWaitLimitAfterTimeoutNs : kWaitLimitNs)) {
+    sh.timed_out = 1;
+    if (lane == 0) {
+      write_failed(b, 0x10);
+      if (!greedy) publish_job(b, nullptr);
+    }
+    __syncwarp();
+    return 0;
+  }
 
   // accept tests (lane i = draft i) and the prefix-terminating scan
   int err = 0;
@@ -529,112 +568,159 @@ __device__ int ChainProblem::request_finalize(Shared& sh, const PosTables& tab, 
     else if (wf.rm[j] == kNegInf || (!greedy && !(wf.rz[j] > 0.f))) err |= 0x04;
   }
   bool acc = false;
-  const double cd = static_cast<double>(c.hi) + static_cast<double>(c.lo);
+  float pa = __int_as_float(0x7fc00000), qa = __int_as_float(0x7fc00000);
   if (lane < nd) {
     if (!x_ok) {
       err |= 0x01;
     } else if (greedy) {
       acc = x == wf.ridx[lane];
-      if (p_at) p_at[static_cast<size_t>(b) * K + lane] = acc ? 1.f : 0.f;
-      if (q_at) q_at[static_cast<size_t>(b) * K + lane] = __int_as_float(0x7fc00000);
+      pa = acc ? 1.f : 0.f;
     } else {
       const int jt = lane, jd = nd + 1 + lane;
-      // p(x) = np / Zp, q(x) = nq / Zq with np, nq in fp64; the test
-      // u q(x) < p(x) is taken as u nq Zp < np Zq (no division)
-      const double np = exp2_nonpos(
-          (static_cast<double>(lx) - static_cast<double>(wf.rm[jt])) * cd);
-      const double nq = exp2_nonpos(
-          (static_cast<double>(dx) - static_cast<double>(wf.rm[jd])) * cd);
-      const double zp = static_cast<double>(wf.rz[jt]), zq = static_cast<double>(wf.rz[jd]);
-      acc = static_cast<double>(ui) * nq * zp < np * zq;
+      // p(x) = np / Zp, q(x) = nq / Zq; the test u q(x) < p(x) is taken as
+      // u nq Zp < np Zq (no division).  First in fp32: np and nq to about
+      // 5e-7 relative, so the two sides carry less than 2e-6 of relative
+      // error between them, and when they differ by more than 4e-6 the
+      // fp32 decision is the fp64 one.  Closer calls, and exponents below
+      // -96 (where u nq Zp could leave the normal range), are decided in
+      // fp64 -- slow on this part, but the fast path takes all but a few
+      // tests per million.
+      float ahp, ahq;
+      const float np32 = exp2_scaled_pair(lx, wf.rm[jt], c, ahp);
+      const float nq32 = exp2_scaled_pair(dx, wf.rm[jd], c, ahq);
+      const float lhs = ui * nq32 * wf.rz[jt], rhs = np32 * wf.rz[jd];
       // Z >= 1 (the maximum's own term), so the reciprocal needs no special cases
-      if (p_at) p_at[static_cast<size_t>(b) * K + lane] = static_cast<float>(np) * rcp_fma(wf.rz[jt]);
-      if (q_at) q_at[static_cast<size_t>(b) * K + lane] = static_cast<float>(nq) * rcp_fma(wf.rz[jd]);
+      if (ahp >= -96.f && ahq >= -96.f && fabsf(lhs - rhs) > 4e-6f * fmaxf(lhs, rhs)) {
+        acc = lhs < rhs;
+        pa = np32 * rcp_fma(wf.rz[jt]);
+        qa = nq32 * rcp_fma(wf.rz[jd]);
+      } else {
+        const double cd = static_cast<double>(c.hi) + static_cast<double>(c.lo);
+        const double np = exp2_nonpos(
+            (static_cast<double>(lx) - static_cast<double>(wf.rm[jt])) * cd);
+        const double nq = exp2_nonpos(
+            (static_cast<double>(dx) - static_cast<double>(wf.rm[jd])) * cd);
+        const double zp = static_cast<double>(wf.rz[jt]), zq = static_cast<double>(wf.rz[jd]);
+        acc = static_cast<double>(ui) * nq * zp < np * zq;
+        pa = static_cast<float>(np) * rcp_fma(wf.rz[jt]);
+        qa = static_cast<float>(nq) * rcp_fma(wf.rz[jd]);
+      }
     }
-  }
-  for (int i = max(lane, nd); i < K; i += 32) {
-    if (p_at) p_at[static_cast<size_t>(b) * K + i] = __int_as_float(0x7fc00000);
-    if (q_at) q_at[static_cast<size_t>(b) * K + i] = __int_as_float(0x7fc00000);
   }
   err = __reduce_or_sync(0xffffffffu, err);
   const unsigned mask = __ballot_sync(0xffffffffu, acc);
   int n = mask == 0xffffffffu ? 32 : __ffs(~mask) - 1;
   n = min(n, nd);
 
+  // a sampled request publishes its draw first -- the draw pass is the
+  // longer path -- then writes its outputs
+  int drew = 0;
+  if (!greedy && lane == 0) {
+    if (!err) {
+      // the draw from norm(max(0, p_n - q_n)) (rejection) or p_nd (bonus)
+      P2Job jb;
+      jb.b = b;
+      jb.n = n;
+      jb.mode = n < nd ? 0 : 1;
+      jb.mp = wf.rm[n];
+      jb.izp = rcp_fma(wf.rz[n]);  // Z >= 1
+      jb.mq = n < nd ? wf.rm[nd + 1 + n] : 0.f;
+      jb.izq = n < nd ? rcp_fma(wf.rz[nd + 1 + n]) : 0.f;
+      jb.c_hi = c.hi;
+      jb.c_lo = c.lo;
+      jb.pos = pos;
+      publish_job(b, &jb);
+      drew = 1;
+    } else {
+      publish_job(b, nullptr);
+    }
+  }
+
   // outputs: the accepted prefix; greedy also the emitted token
+  if (lane < nd) {
+    if (p_at) p_at[static_cast<size_t>(b) * K + lane] = pa;
+    if (q_at) q_at[static_cast<size_t>(b) * K + lane] = qa;
+  }
+  for (int i = max(lane, nd); i < K; i += 32) {
+    if (p_at) p_at[static_cast<size_t>(b) * K + i] = __int_as_float(0x7fc00000);
+    if (q_at) q_at[static_cast<size_t>(b) * K + i] = __int_as_float(0x7fc00000);
+  }
   for (int i = lane; i <= K; i += 32) {
     int v = -1;
     if (!err) {
-      if (i < n) v = tokens[static_cast<size_t>(b) * K + i];
+      if (i < n) v = x;  // i < n <= nd <= 32: lane i holds draft i
       else if (i == n && greedy) v = wf.ridx[n];
     }
     out_tokens[static_cast<size_t>(b) * (K + 1) + i] = v;
   }
-  if (!greedy && !err) {
-    // the draw's segment sums start at -1: the draw finalize waits for
-    // every one of them to be written (sums are >= 0).  Each lane marks
-    // exactly the sums it polls later (16 consecutive ones of each page of
-    // 512), with GPU-scope stores, so its polls cannot see an older value.
-    const int nseg = ipr2 * segs_per_chunk();
-    float* ss = ws.segsums + static_cast<size_t>(b) * nseg;
-    for (int g = 0; g * kPageSeg < nseg; ++g)
-      for (int k = 0; k < 16; ++k) {
-        const int i = g * kPageSeg + lane * 16 + k;
-        if (i < nseg)
-          asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(ss + i), "f"(-1.f) : "memory");
-      }
-  }
-  __syncwarp();  // every lane's outputs before lane 0's release below
-  int drew = 0;
+  __syncwarp();  // every lane's outputs before a later draw finalize overwrites one
   if (lane == 0) {
     out_len[b] = err ? 0 : n + 1;
     accept_len[b] = err ? 0 : n;
     if (err) record_error(&ws.hdr->error, err);
-    ws.tickets[b] = 0u;  // ready for the next call
-    if (!greedy) {
-      // Every sampled request puts exactly one entry in the draw list -- its
-      // draw, or -1 when the request failed -- so the list's final length
-      // is the number of sampled requests, known from the start.
-      int entry = -1;
-      if (!err) {
-        // the draw from norm(max(0, p_n - q_n)) (rejection) or p_nd (bonus)
-        P2Job jb;
-        jb.b = b;
-        jb.n = n;
-        jb.mode = n < nd ? 0 : 1;
-        jb.mp = wf.rm[n];
-        jb.izp = rcp_fma(wf.rz[n]);  // Z >= 1
-        jb.mq = n < nd ? wf.rm[nd + 1 + n] : 0.f;
-        jb.izq = n < nd ? rcp_fma(wf.rz[nd + 1 + n]) : 0.f;
-        jb.c_hi = c.hi;
-        jb.c_lo = c.lo;
-        jb.pad[0] = jb.pad[1] = jb.pad[2] = 0;
-        jobs[b] = jb;
-        entry = b + 1;
-      }
-      fence_acq_rel_gpu();  // the job and the outputs before the entry
-      const unsigned d = atomicAdd(&ws.hdr->draw_reserve, 1u);
-      st_relaxed(ws.draws + d, entry);
-      drew = entry > 0 ? 1 : 0;
-    }
   }
   // 1 when a draw was published (its draw finalize follows its draw pass)
   return __shfl_sync(0xffffffffu, drew, 0);
 }
 
-// Lane l's 16 segment sums of page g (segments [512 g + 16 l, +16)), zero
-// beyond nseg (a multiple of 4).
-__device__ __forceinline__ void load_page(const float* ss, int nseg, int g, int lane, float* v) {
+// Lane l's 16 stored segment sums of page g (segments [512 g + 16 l, +16)),
+// as words; beyond nseg (a multiple of 4) the encoding of zero.
+__device__ __forceinline__ void load_page_words(const unsigned* ss, int nseg, int g, int lane,
+                                                unsigned* w) {
   const int i0 = g * kPageSeg + lane * 16;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (i0 + 4 * q < nseg) f = __ldcg(reinterpret_cast<const float4*>(ss + i0 + 4 * q));
-    v[4 * q] = f.x;
-    v[4 * q + 1] = f.y;
-    v[4 * q + 2] = f.z;
-    v[4 * q + 3] = f.w;
+    uint4 f = make_uint4(0x80000000u, 0x80000000u, 0x80000000u, 0x80000000u);
+    if (i0 + 4 * q < nseg) f = ld_relaxed_v4(ss + i0 + 4 * q);
+    w[4 * q] = f.x;
+    w[4 * q + 1] = f.y;
+    w[4 * q + 2] = f.z;
+    w[4 * q + 3] = f.w;
   }
+}
+
+// The same, polled until every sum of the page is written (bounded; false
+// in every lane when the wait expired), decoded into v.
+__device__ __forceinline__ bool poll_page(const unsigned* ss, int nseg, int g, int lane, float* v,
+                                          uint64_t limit) {
+  const uint64_t t0 = globaltimer_ns();
+  const int i0 = g * kPageSeg + lane * 16;
+  unsigned w[16];
+  load_page_words(ss, nseg, g, lane, w);
+  unsigned backoff = 64;
+  bool ok = true;
+  for (;;) {
+    int missing = 0;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) missing += w[k] == 0u;
+    if (__all_sync(0xffffffffu, missing == 0)) break;
+    if (globaltimer_ns() - t0 > limit) {
+      ok = false;
+      break;
+    }
+    __nanosleep(backoff);
+    backoff = min(backoff * 2u, 128u);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (w[4 * q] == 0u || w[4 * q + 1] == 0u || w[4 * q + 2] == 0u || w[4 * q + 3] == 0u) {
+        const uint4 f = ld_relaxed_v4(ss + i0 + 4 * q);
+        w[4 * q] = f.x;
+        w[4 * q + 1] = f.y;
+        w[4 * q + 2] = f.z;
+        w[4 * q + 3] = f.w;
+      }
+  }
+#pragma unroll
+  for (int k = 0; k < 16; ++k) v[k] = dec_seg(w[k]);
+  return ok;
+}
+
+// Lane l's 16 segment sums of page g, already written, decoded into v.
+__device__ __forceinline__ void load_page(const unsigned* ss, int nseg, int g, int lane, float* v) {
+  unsigned w[16];
+  load_page_words(ss, nseg, g, lane, w);
+#pragma unroll
+  for (int k = 0; k < 16; ++k) v[k] = dec_seg(w[k]);
 }
 
 // The draw from the weights of the draw pass: S = the sum of the segment
@@ -642,18 +728,21 @@ __device__ __forceinline__ void load_page(const float* ss, int nseg, int g, int 
 // (pages of 512 segments, then the lane's block of 16, then the segment),
 // then the token within it.  Running sums are float pairs; the search goes
 // in ascending token order throughout, as the inverse CDF does.
-__device__ void ChainProblem::draw_finalize(int b, int lane, WarpFin& wf) const {
-  const P2Job jb = load_job(b);
+__device__ void ChainProblem::draw_finalize(Shared& sh, const PosTables& tab, int pos, int lane,
+                                            WarpFin& wf) const {
+  const int b = info_req(tab.info[pos]);
+  const P2Job jb = load_job(tab, pos);
   const int n = jb.n, mode = jb.mode;
   const int nseg = ipr2 * segs_per_chunk();
-  float* ss = ws.segsums + static_cast<size_t>(b) * nseg;
+  unsigned* ss = reinterpret_cast<unsigned*>(ws.segsums) + static_cast<size_t>(b) * nseg;
   const float u = uniforms[static_cast<size_t>(b) * (K + 1) + K];
   const char* pr = trow(b, n);
   const char* qr = mode == 0 ? drow(b, n) : nullptr;
   ResidParams rp{jb.mp, jb.izp, jb.mq, jb.izq, Scale2{jb.c_hi, jb.c_lo}, mode};
   const int npages = (nseg + kPageSeg - 1) / kPageSeg;
   int token = -1;
-  for (int attempt = 0; attempt < 2 && token < 0; ++attempt) {
+  bool timed_out = false;
+  for (int attempt = 0; attempt < 2 && token < 0 && !timed_out; ++attempt) {
     if (attempt == 1) {
       if (mode != 0) break;
       // a residual of zero mass (rounding only): draw from p_n instead --
@@ -667,7 +756,7 @@ __device__ void ChainProblem::draw_finalize(int b, int lane, WarpFin& wf) const 
         load8(pr, es, bulk, t0, 0, xq);
         const float ls = resid_weights8(xp, xq, t0, V, rp, w);
         const float inc = warp_incl_scan_rn(ls, lane);
-        if (lane == 31) __stcg(ss + k, inc);
+        if (lane == 31) __stcg(ss + k, enc_seg(inc));
       }
       __threadfence_block();
       __syncwarp();
@@ -676,7 +765,17 @@ __device__ void ChainProblem::draw_finalize(int b, int lane, WarpFin& wf) const 
     float v[16];
     DF S{0.f, 0.f};
     for (int g = 0; g < npages; ++g) {
-      load_page(ss, nseg, g, lane, v);
+      // the first pass waits for the draw pass's sums to be written
+      if (attempt == 0) {
+        if (!poll_page(ss, nseg, g, lane, v,
+                       sh.timed_out ? kWaitLimitAfterTimeoutNs : kWaitLimitNs)) {
+          sh.timed_out = 1;
+          timed_out = true;
+          break;
+        }
+      } else {
+        load_page(ss, nseg, g, lane, v);
+      }
       DF bs{0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < 16; ++j) bs = df_add(bs, v[j]);
@@ -688,6 +787,7 @@ __device__ void ChainProblem::draw_finalize(int b, int lane, WarpFin& wf) const 
       S = df_add(S, tot);
     }
     __syncwarp();
+    if (timed_out) break;
     if (!(S.hi > 0.f)) continue;
     const DF target = df_mul(u, S);
     // the page holding target (target < S, so there is one)
@@ -784,14 +884,16 @@ __device__ void ChainProblem::draw_finalize(int b, int lane, WarpFin& wf) const 
       for (int i = 0; i <= K; ++i) out_tokens[static_cast<size_t>(b) * (K + 1) + i] = -1;
       out_len[b] = 0;
       accept_len[b] = 0;
-      record_error(&ws.hdr->error, 0x04);
+      record_error(&ws.hdr->error, timed_out ? 0x10 : 0x04);
     }
-    ws.tickets[kDrawTicketBase + b] = 0u;
   }
   __syncwarp();
-  // leave the segment sums zero: any part of the workspace may serve another
-  // call's chunk partials, which must start at zero
-  for (int k = lane; k < nseg; k += 32) ss[k] = 0.f;
+  // leave the segment sums and the draw's record zero: any part of the
+  // workspace may serve another call's chunk partials, which must start at
+  // zero, and every claim of this draw has read the record (its chunks are
+  // all in)
+  for (int k = lane; k < nseg; k += 32) ss[k] = 0u;
+  if (lane < 3) jobs[static_cast<size_t>(b) * kJobWords + lane] = 0ull;
   __syncwarp();
 }
 

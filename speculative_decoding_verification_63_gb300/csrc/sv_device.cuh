@@ -213,6 +213,22 @@ __device__ __forceinline__ float scaled_arg(float x, float m, Scale2 c) {
   return fmaf(d, c.hi, d * c.lo);
 }
 
+// 2^((x - m) c) for x <= m to about 5e-7 relative, whatever the size of the
+// exponent: the exponent is carried as an unevaluated pair -- x - m exactly
+// (TwoSum), the product's rounding error by FMA -- the high part goes
+// through ex2.approx and the low part (below 2^-23 of the high part) to
+// first order.  a_hi returns the high part (exponents below -126 flush to
+// zero).
+__device__ __forceinline__ float exp2_scaled_pair(float x, float m, Scale2 c, float& a_hi) {
+  const float d = x - m;
+  const float bv = d - x;
+  const float d_lo = (x - (d - bv)) + (-m - bv);
+  const float p = d * c.hi;
+  const float lo = fmaf(d, c.hi, -p) + fmaf(d_lo, c.hi, d * c.lo);
+  a_hi = p;
+  return fast_exp2(p) * fmaf(lo, 0.693147180559945f, 1.f);
+}
+
 // ------------------------------------------------- (max, sum) combination
 
 // Online-softmax pair: the row max m and s = sum 2^((x - m) c).  m = -inf
@@ -420,6 +436,21 @@ __device__ __forceinline__ float ld_relaxed_f32(const float* p) {
 }
 __device__ __forceinline__ void st_relaxed(int* p, int v) {
   asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Release store at GPU scope: the thread's earlier writes (and those it has
+// observed) become visible no later than the stored value.
+__device__ __forceinline__ void st_release(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Four consecutive 32-bit words read with one relaxed GPU-scope load (each
+// word single-copy atomic), for polling several words per round trip.
+__device__ __forceinline__ uint4 ld_relaxed_v4(const unsigned* p) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
 }
 __device__ __forceinline__ void fence_acq_rel_gpu() {
   asm volatile("fence.acq_rel.gpu;" ::: "memory");

@@ -1,7 +1,7 @@
 // sv_kernel.cuh -- the persistent verification kernel, generic over the
 // problem (chain or tree).
 //
-// One CTA per SM, five or six warp roles (control warps first, so that the warp
+// One CTA per SM, warp roles (control warps first, so that the warp
 // schedulers, which favour lower warp ids, serve them ahead of the
 // always-ready consumers):
 //   warp  0      producer: moves chunks into the 4-stage ring with 1-D bulk
@@ -17,34 +17,32 @@
 //                one sentinel per consumer group.
 //   warp  1      bookkeeper: takes result slots in order, combines the 8
 //                per-warp partials of a chunk (max first, one rescale, a
-//                sum) or keeps the residual segment sums, stores them and
-//                appends the chunk's ticket to the booked queue.
-//   warp  2      ticket warp: takes booked chunks in lane-parallel batches,
-//                fences, bumps the tickets; a completed request or residual
-//                draw joins the finalize list.
+//                sum) or keeps the residual segment sums and stores them;
+//                without control CTAs it also appends the chunk's ticket to
+//                the booked queue.
+//   warp  2      ticket warp (problems without control CTAs): takes booked
+//                chunks in lane-parallel batches, fences, bumps the tickets;
+//                a completed request joins the finalize list.
 //   warp  6      draw scout (problems with draw passes; otherwise the
-//                fourth finalizer): takes draw-pass claims from a global counter
-//                (claim g is chunk g % ipr2 of the (g / ipr2)-th entry of the
-//                global draw list, where every sampled request's finalize
-//                puts one entry: its draw, or -1 if it failed), waits for the
-//                entry, fetches the job, plans the chunk and leaves it in the
-//                mailbox; claims beyond the number of sampled requests lapse.
-//   warps 3..5   finalizers (3..6 without draw passes): take finalize-list
-//                entries (each warp on its own, or the four together for
-//                problems that need a group) while the consumers keep
-//                streaming.
+//                fourth finalizer): walks the CTA's static share of the
+//                draw-pass claims, waits for each claimed draw to be
+//                published, plans the chunk and leaves it in the mailbox.
+//   warps 3..5   finalizers (3..6 without draw passes; problems without
+//                control CTAs): take finalize-list entries (each warp on its
+//                own, or the four together for problems that need a group)
+//                while the consumers keep streaming.
 //   warps 7..22  consumers, in two groups of eight that take alternate
 //                chunks (so each group has two chunk times per chunk): each
 //                warp reduces its eighth of the chunk, releases the stage as
 //                soon as the data is in registers, and posts its partial
 //                into the result ring.
 // Every hand-off is an mbarrier or a shared counter polled with back-off;
-// every wait is bounded.  The one wait on other CTAs -- a draw-pass claim
-// waiting for its draw -- only ever waits on CTAs that are running: the
-// grid never exceeds the SM count and a CTA holds the whole of an SM, and
-// a draw depends only on main-pass chunks and on finalizes, which never
-// wait on other CTAs.
-//
+// every wait is bounded.  The waits on other CTAs -- a finalize on its
+// request's chunks, a scout on its claimed draw, a draw finalize on its
+// draw's chunks -- only ever wait on CTAs that are running: the grid never
+// exceeds the SM count and a CTA holds the whole of an SM, and none of the
+// awaited work waits on the waiter.
+
 // A problem type P provides:
 //   int n_req, ipr, chunk_el, es, V; bool bulk; Ws ws;
 //   static constexpr int kAuxBytes       per-position aux table (0, 8, 16)
@@ -54,11 +52,13 @@
 //   void fill_stage(const PosTables&, int row_local, StageMeta&, ResMeta&)
 //        -> a main-pass chunk: kind, scale, source, ticket fields (producer)
 //   void fill_resid(const P2Job&, int chunk, StageMeta&, ResMeta&) const
-//        -> a draw-pass chunk (producer)
+//        -> a draw-pass chunk (scout)
 //   int ipr2                     chunks per draw
-//   P2Job load_job(int b) const  the draw published for request b
-//   void store_segsums(const ResMeta&, int lane, float4) const
-//        -> the bookkeeper's store of a draw-pass chunk's segment sums
+//   int poll_job(const PosTables&, int d, uint64_t limit, P2Job&) const
+//        -> the draw at position d, polled until published (1), failed (0)
+//           or the wait expired (-1)
+//   void store_segsums_warp(int slot, int w, float4) const
+//        -> the bookkeeper's store of consumer warp w's segment sums
 //   float4 consume(const StageMeta&, const unsigned char* stage,
 //                  uint64_t* empty_bar, int ctid, int lane) const
 //        (ctid: thread index within the consumer group)
@@ -66,7 +66,6 @@
 //                      WarpFin&) const     (kWarpFinalize)
 //   void finalize(Shared&, const PosTables&, int code, int ftid) const
 //                                          (!kWarpFinalize, all 4 warps)
-//   void last_cta_reset() const  (the last CTA to finish, after all others)
 //   static constexpr bool kHasDirectFin  some requests need no main-pass rows
 //   bool direct_fin(const PosTables&, int pos) const
 //        -> request at pos goes straight to the finalize list (kHasDirectFin)
@@ -114,35 +113,6 @@ __device__ __forceinline__ unsigned vload(const unsigned& x) {
 __device__ __forceinline__ void flag_timeout(Shared& sh, int* err) {
   sh.timed_out = 1;
   record_error(err, 0x10);
-}
-
-// Wait, bounded, until the ticket counter reaches `need`: lane 0 polls it
-// with acquire loads and back-off, then the warp synchronises, so every
-// lane's later loads see what the completing chunks published.  Returns
-// false in every lane when the wait expired.
-__device__ __forceinline__ bool wait_ticket(Shared& sh, const unsigned* ticket, unsigned need,
-                                            int lane) {
-  int ok = 1;
-  if (lane == 0 && ld_acquire(ticket) != need) {
-    const uint64_t t0 = globaltimer_ns();
-    unsigned backoff = 32;
-    ok = 0;
-    for (;;) {
-      __nanosleep(backoff);
-      if (ld_acquire(ticket) == need) {
-        ok = 1;
-        break;
-      }
-      if (globaltimer_ns() - t0 > wait_limit(sh)) {
-        sh.timed_out = 1;
-        break;
-      }
-      backoff = min(backoff * 2u, 256u);
-    }
-  }
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  __syncwarp();
-  return ok != 0;
 }
 
 // Control CTAs (problems with kCtrl): the last n_ctrl CTAs of the grid
@@ -322,27 +292,35 @@ __device__ void producer_loop(const P& prob, Shared& sh, const PosTables& tab,
   __syncwarp();
 }
 
-// The draw scout (lane 0 of its warp): takes draw-pass claims from the
-// global counter, waits for the claimed draw to be published, fetches its
-// job, plans the chunk and leaves the record in the shared mailbox for the
-// producer.  Claim g is chunk g % ipr2 of the (g / ipr2)-th entry of the
-// draw list, where every sampled request's finalize puts one entry (its
-// draw, or -1 if it failed); claims beyond the number of sampled requests
-// lapse and end the scout.  All its waits on global memory happen here, off
-// the producer's path.
+// The draw scout (lane 0 of its warp): walks this CTA's draw-pass claims,
+// waits for each claimed draw to be published, plans the chunk and leaves
+// the record in the shared mailbox for the producer.  Claim g is chunk
+// g % ipr2 of the draw at position g / ipr2 (sampled requests hold the
+// first positions, in the order their rows stream).  The claims continue
+// the main pass's round robin: claim g goes to the streaming CTA that
+// main-pass item n_items + g would go to, so every CTA streams the same
+// number of chunks, to within one, and no counter is shared.  The scout
+// polls each draw's record itself; a failed request's draw has no chunks
+// (the last of its claims clears the record).  All its waits on global
+// memory happen here, off the producer's path.
 template <class P>
-__device__ void scout_loop(const P& prob, Shared& sh) {
+__device__ void scout_loop(const P& prob, Shared& sh, const PosTables& tab) {
   if constexpr (P::kHasDraws) {
     const int lane = threadIdx.x & 31;
-    WsHeader* hdr = prob.ws.hdr;
-    int* err = &hdr->error;
+    int* err = &prob.ws.hdr->error;
     const unsigned cap = static_cast<unsigned>(sh.n_draw_cap);
+    const unsigned G = gridDim.x - n_ctrl_of(prob);
+    const unsigned n_claims = cap * static_cast<unsigned>(prob.ipr2);
+    const unsigned n_items =
+        static_cast<unsigned>(tab.rstart[sh.n_pos]) * static_cast<unsigned>(prob.ipr);
     if (lane == 0 && cap > 0) {
       unsigned tail = 0;
       unsigned cached_d = 0xffffffffu;
-      bool cached_failed = false;
+      int cached = 0;  // 1: a draw, 0: the request failed
       P2Job job{};
-      for (;;) {
+      // the first claim g with (n_items + g) % G == this CTA
+      const unsigned first = (blockIdx.x + G - n_items % G) % G;
+      for (unsigned g = first; g < n_claims; g += G) {
         // room in the mailbox
         if (tail - vload(sh.mb_head) >= static_cast<unsigned>(kMbCap)) {
           const uint64_t t0 = globaltimer_ns();
@@ -359,35 +337,19 @@ __device__ void scout_loop(const P& prob, Shared& sh) {
             break;
           }
         }
-        const unsigned g = atomicAdd(&hdr->work_counter, 1u);
         const unsigned d = g / static_cast<unsigned>(prob.ipr2);
-        if (d >= cap) break;
         if (d != cached_d) {
-          int e = ld_relaxed(prob.ws.draws + d);
-          if (e == 0) {
-            const uint64_t t0 = globaltimer_ns();
-            unsigned backoff = 32;
-            while (e == 0) {
-              if (globaltimer_ns() - t0 > wait_limit(sh)) break;
-              __nanosleep(backoff);
-              backoff = min(backoff * 2u, 256u);
-              e = ld_relaxed(prob.ws.draws + d);
-            }
-            if (e == 0) {
-              flag_timeout(sh, err);
-              break;
-            }
+          cached = prob.poll_job(tab, static_cast<int>(d), wait_limit(sh), job);
+          if (cached < 0) {
+            flag_timeout(sh, err);
+            break;
           }
           cached_d = d;
-          cached_failed = e < 0;
-          if (!cached_failed) {
-            // read the entry again with acquire (the job was published
-            // before it), then fetch the job
-            e = ld_acquire(prob.ws.draws + d);
-            job = prob.load_job(e - 1);
-          }
         }
-        if (cached_failed) continue;  // a failed request's draw has no chunks
+        if (cached == 0) {  // a failed request's draw has no chunks
+          prob.failed_claim(tab, static_cast<int>(d));
+          continue;
+        }
         PlanRec rec;
         StageMeta& mt = rec.s.m;
         ResMeta& rm = rec.s.r;
@@ -397,7 +359,7 @@ __device__ void scout_loop(const P& prob, Shared& sh) {
         prob.fill_resid(job, static_cast<int>(g % static_cast<unsigned>(prob.ipr2)), mt, rm);
         rm.item = mt.item;
         mt.slot = rm.slot;
-              rm.kind = mt.kind;
+        rm.kind = mt.kind;
         rm.c_hi = mt.c_hi;
         rm.c_lo = mt.c_lo;
         uint4* dst = reinterpret_cast<uint4*>(&sh.mb[tail % kMbCap]);
@@ -457,11 +419,12 @@ __device__ void bookkeeper_loop(const P& prob, Shared& sh) {
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.res_free[rs]);
     if constexpr (P::kCtrl) {
-      // Control CTAs poll: the results go straight to the workspace (words
-      // the pollers check themselves), then a relaxed count that tells them
-      // when to look.  No fence, no queue, nothing waits here.
+      // Control CTAs poll: the results go straight to the workspace, as
+      // words the pollers check themselves.  No count, no fence, no queue,
+      // nothing waits here.
       if (rm.kind == KIND_RESID_PASS) {
-        if (lane < kGroupWarps) prob.store_segsums_warp(rm.slot, lane, p);
+        if constexpr (P::kHasDraws)
+          if (lane < kGroupWarps) prob.store_segsums_warp(rm.slot, lane, p);
       } else {
         float2 tot;
         if (rm.kind == KIND_ARGMAX) {
@@ -474,14 +437,9 @@ __device__ void bookkeeper_loop(const P& prob, Shared& sh) {
         }
         if (lane == 0) prob.store_partial(rm.slot, rm.kind, tot);
       }
-      __syncwarp();
-      if (lane == 0) red_relaxed_add(prob.ws.tickets + rm.tkt, 1u);
       continue;
     }
-    if (rm.kind == KIND_RESID_PASS) {
-      // draw-pass chunk: the segment sums of the consumer warps, in order
-      if constexpr (P::kHasDraws) prob.store_segsums(rm, lane, p);
-    } else {
+    {
       float2 tot;
       if (rm.kind == KIND_ARGMAX) {
         const VI v = warp_reduce_vi(VI{p.x, lane < kGroupWarps ? __float_as_int(p.y)
@@ -590,16 +548,7 @@ __device__ void ticketer_loop(const P& prob, Shared& sh, const PosTables& tab) {
     __threadfence_block();  // the entries (and the bookkeeper's stores) before reading them
     const int nb = static_cast<int>(min(tail - head, 32u));
     const int4 e = lane < nb ? sh.bq[(head + lane) % kBqCap] : make_int4(0, 0, 0, 0);
-    if constexpr (P::kCtrl) {
-      // Control CTAs poll the tickets, so nothing here needs the counts: one
-      // release reduction per distinct ticket of the batch (lanes with the
-      // same ticket merged), no fence and no round trip.  The release makes
-      // the partials the bookkeeper stored (seen through the queue) visible
-      // before the count that covers them.
-      const unsigned same = __match_any_sync(0xffffffffu, lane < nb ? e.x : -1);
-      if (lane < nb && lane == __ffs(same) - 1)
-        red_release_add(&prob.ws.tickets[e.x], static_cast<unsigned>(__popc(same)));
-    } else {
+    {
       fence_acq_rel_gpu();  // the partials (stored by the bookkeeper) -> GPU scope before the tickets
       bool done = false;
       if (lane < nb) {
@@ -775,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const P prob) {
     sh.bq_tail = sh.bq_head = 0u;
     sh.tk_done = 0u;
     sh.p_it = 0u;
-    if (P::kHasDraws) sh.mb_tail = sh.mb_head = sh.sc_done = 0u;
+    if constexpr (P::kHasDraws) sh.mb_tail = sh.mb_head = sh.sc_done = 0u;
     sh.fin_cmd = -1;
     sh.n_draw_cap = 0;
   }
@@ -789,36 +738,17 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const P prob) {
   } else if (threadIdx.x < kTkBase) {
     bookkeeper_loop(prob, sh);
   } else if (threadIdx.x < kFinBase) {
-    if (!P::kCtrl) ticketer_loop(prob, sh, tab);  // control CTAs poll the counts themselves
+    if (!P::kCtrl) ticketer_loop(prob, sh, tab);  // control CTAs poll the data words themselves
   } else if (threadIdx.x < kConsBase) {
-    if (P::kHasDraws && threadIdx.x >= kScBase) scout_loop(prob, sh);
+    if (P::kHasDraws && threadIdx.x >= kScBase) scout_loop(prob, sh, tab);
     else if (!P::kCtrl) finalizer_loop(prob, sh, tab);
   } else {
     consumer_loop(prob, sh, stages);
   }
-  __syncthreads();
-  // the last CTA to finish leaves the shared counters zeroed for the next call
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned d = atomicAdd(&prob.ws.hdr->done_ctas, 1u);
-    sh.is_last = d + 1u == gridDim.x ? 1 : 0;
-    if (sh.is_last) __threadfence();
-  }
-  __syncthreads();
-  if (sh.is_last) {
-    WsHeader* hdr = prob.ws.hdr;
-    const int nd = min(static_cast<int>(*reinterpret_cast<volatile unsigned*>(&hdr->draw_reserve)),
-                       prob.n_req);
-    for (int i = threadIdx.x; i < nd; i += kThreads) prob.ws.draws[i] = 0;
-    prob.last_cta_reset();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      hdr->work_counter = 0u;
-      hdr->done_ctas = 0u;
-      hdr->draw_reserve = 0u;
-      __threadfence();
-    }
-  }
+  // Nothing to reset at the end: every word of the workspace this call
+  // wrote is cleared by the role that read it last (partials by their
+  // finalize, segment sums and draw records by the draw finalize, a failed
+  // draw's record by its last claim), so a CTA just exits.
 }
 
 }  // namespace sv

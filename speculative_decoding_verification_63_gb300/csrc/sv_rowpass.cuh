@@ -69,22 +69,19 @@ constexpr int kFinResid = 0x40000000;  // finalize-list flag: a residual draw (r
 constexpr int kDrawTicketBase = 1024;  // draw tickets follow the request tickets (SV_MAX_B)
 
 struct WsHeader {
-  unsigned int work_counter;  // draw-pass chunks claimed
-  unsigned int done_ctas;
+  unsigned int pad0[2];
   int error;
-  unsigned int draw_reserve;  // entries of the draw list reserved so far
-  unsigned int pad[4];
+  unsigned int pad[5];
 };
 
 // Device view of the caller's workspace.
 struct Ws {
   WsHeader* hdr;
   unsigned int* tickets;  // [2 SV_MAX_B] chunk counters: requests, then their draws
-  int* draws;             // [SV_MAX_B] draw list: request id + 1, 0 = not yet written
   float2* partials;       // [rows_max * ipr] one (max, sum) / (max, argmax) per chunk
   float* segsums;         // [B * ipr2 * segments per chunk] residual segment sums
   float* scratch;         // per-request residual rows (tree walk) [B][2][V]
-  void* jobs;             // residual draws [SV_MAX_B]
+  void* jobs;             // residual draws [SV_MAX_B][kJobWords]
 };
 
 // A residual / bonus draw (CMU 15-779 Lecture 17, sec. 2.3-2.4): request b,
@@ -92,10 +89,28 @@ struct Ws {
 // statistics of p_n and q_n, and the temperature scale.
 struct P2Job {
   int b, n, mode;
+  int pos;  // the request's position in the processing order
   float mp, izp, mq, izq;
   float c_hi, c_lo;
-  int pad[3];
 };
+
+// A published draw as the workspace holds it: kJobWords 64-bit words per
+// request, each never zero once written, so the draw-pass scouts poll the
+// words themselves -- no flag, no fence.
+//   w0 = bits(1/Z_p) | bits(m_p) << 32      1/Z_p in (0, 1]: low word nonzero
+//   w1 = bits(1/Z_q) | bits(m_q) << 32      low word 0x80000000 when unused
+//   w2 = (1 + n + (mode << 8)) | failed << 32
+// The temperature scale is not stored: every CTA holds it per position.
+constexpr int kJobWords = 4;  // three used, one spare (32 bytes per request)
+
+// Draw-pass segment sums are kept sign-flipped in the workspace: a sum is
+// >= 0 (negative zero is stored as +0), so a stored sum is never the zero
+// word, and zero marks a sum not yet written this call.
+__device__ __forceinline__ unsigned enc_seg(float s) {
+  const unsigned u = __float_as_uint(s);
+  return (u == 0x80000000u ? 0u : u) ^ 0x80000000u;
+}
+__device__ __forceinline__ float dec_seg(unsigned w) { return __uint_as_float(w ^ 0x80000000u); }
 
 struct StageMeta {
   int item;      // -1: no more work
@@ -179,7 +194,6 @@ struct __align__(16) Shared {
   int n_pos;
   int n_draw_cap;   // at most this many draws can be published (sampled requests)
   int timed_out;  // a bounded wait of this CTA expired: later waits are short
-  int is_last;    // this CTA finished last
   FinScratch fin;
   WarpFin wfin[kFinWarps];
   PlanRec mb[kMbCap];          // scout -> producer: planned draw chunks

@@ -177,7 +177,6 @@ struct TreeProblem {
 
   __device__ void finalize(Shared& sh, const PosTables& tab, int pos, int ftid) const;
   __device__ void finalize_warp(Shared&, const PosTables&, int, int, WarpFin&) const {}
-  __device__ void last_cta_reset() const {}
 };
 
 // Weights for the tree's inverse-CDF draw: either p_node (unnormalised

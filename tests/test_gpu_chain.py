@@ -178,6 +178,27 @@ def test_data_errors_are_reported_per_request():
             prefix_tokens=good["tokens"])
 
 
+def test_failed_requests_leave_the_workspace_clean():
+    """Sampled requests that fail publish a failed draw, whose record the
+    last of its draw-pass claims clears: the next call on the same
+    workspace, with no re-initialisation, must see none of it."""
+    bad = wl.make_chain(3, B=12, V=20_000, seed=18, greedy="none")
+    for b in (1, 4, 7):
+        bad["target"][b, 3, 500] = 0x7FC0     # NaN: request b fails
+    bad["tokens"][10, 0] = 20_000             # out of range: request 10 fails
+    ws = sv.workspace(sv.sv_chain_workspace_bytes(12, 6, 20_000, sv.SV_BF16), "cuda", "clean")
+    got = run_chain(bad, ws=ws)
+    assert list(got["out_len"][[1, 4, 7, 10]]) == [0, 0, 0, 0]
+    st, flags = sv.sv_get_error(ws)
+    assert st == sv.SV_EDATA
+    for seed in (19, 20):
+        good = wl.make_chain(3, B=12, V=20_000, seed=seed, greedy="none")
+        compare(run_chain(good, ws=ws), oracle.verify_chain_inputs(good), 12,
+                prefix_tokens=good["tokens"])
+    st, flags = sv.sv_get_error(ws)
+    assert st == sv.SV_OK and flags == 0
+
+
 def test_greedy_with_nan_draft_rows_is_fine():
     """Greedy requests never read draft rows."""
     inp = wl.make_chain(3, B=4, V=4000, greedy="all", seed=17)
