@@ -59,13 +59,6 @@ struct ChainProblem {
   const float2* topk_mz;     // [B (2K+1)] (m, Z) over those logits
   Ws ws;
 
-  // kind of request b, or -1 if its scalar arguments are invalid
-  __device__ int classify(int b, int& nd) const {
-    nd = num_drafts ? num_drafts[b] : K;
-    return chain_kind(nd, temperature[b], top_k ? top_k[b] : 0, K, V, max_topk,
-                      draft != nullptr);
-  }
-
   __device__ void write_failed(int b, int flag) const {
     for (int i = 0; i <= K; ++i) out_tokens[static_cast<size_t>(b) * (K + 1) + i] = -1;
     out_len[b] = 0;
@@ -77,23 +70,41 @@ struct ChainProblem {
     record_error(&ws.hdr->error, flag);
   }
 
+  // Before the launch may read its inputs (the wait on the preceding work):
+  // ask L2 for the lines of the per-request arguments the preamble reads.
+  // A prefetch is only a hint and L2 is the point of coherence, so it can
+  // return no stale value.
+  __device__ void prefetch_args(int lane) const {
+    if (32 * lane >= n_req) return;
+    prefetch_l2(temperature + 32 * lane);
+    if (num_drafts) prefetch_l2(num_drafts + 32 * lane);
+    if (top_k) prefetch_l2(top_k + 32 * lane);
+  }
+
   // Processing order: sampled requests first (their draw pass should overlap
-  // the rest of the main pass), then greedy ones.  rows: greedy nd+1,
-  // sampled 2nd+1; top-k requests read no rows here (the top-k pass has
-  // reduced them to lists) and go straight to their finalize.
-  __device__ void preamble(Shared& sh, PosTables& tab, int4* scan_tmp) const {
-    const int per = (n_req + kThreads - 1) / kThreads;
-    const int lo = min(static_cast<int>(threadIdx.x) * per, n_req);
+  // the rest of the main pass), then greedy ones, each in request order.
+  // rows: greedy nd+1, sampled 2nd+1; top-k requests read no rows here (the
+  // top-k pass has reduced them to lists) and go straight to their
+  // finalize.  Warp 0 alone: lane l takes a contiguous block of requests,
+  // classifies them in one load pass (its classification goes to
+  // `scratch`, the chunk ring, idle until the preamble ends), a warp scan
+  // places the blocks, and a second pass over the scratch fills the
+  // position tables.  The other warps go straight to the barrier after it.
+  __device__ void preamble(Shared& sh, PosTables& tab, int4*, unsigned char* scratch) const {
+    if (threadIdx.x >= 32) return;
+    const int lane = threadIdx.x;
+    int4* req = reinterpret_cast<int4*>(scratch);  // per request: kind, nd, bits of t
+    const int per = (n_req + 31) / 32;
+    const int lo = min(lane * per, n_req);
     const int hi = min(lo + per, n_req);
     int4 cnt = make_int4(0, 0, 0, 0);  // sampled n, sampled rows, other n, other rows
+#pragma unroll 4
     for (int b = lo; b < hi; ++b) {
-      int nd;
-      const int kind = classify(b, nd);
-      if (kind < 0) {
-        cnt.z += 1;
-        continue;
-      }
-      const int rows = kind == KIND_ARGMAX ? nd + 1 : (kind == KIND_TOPK ? 0 : 2 * nd + 1);
+      const int nd = num_drafts ? num_drafts[b] : K;
+      const float t = temperature[b];
+      const int kind = chain_kind(nd, t, top_k ? top_k[b] : 0, K, V, max_topk, draft != nullptr);
+      req[b] = make_int4(kind, nd, __float_as_int(t), 0);
+      const int rows = kind < 0 ? 0 : (kind == KIND_ARGMAX ? nd + 1 : (kind == KIND_TOPK ? 0 : 2 * nd + 1));
       if (kind == KIND_SOFTMAX) {
         cnt.x += 1;
         cnt.y += rows;
@@ -102,12 +113,25 @@ struct ChainProblem {
         cnt.w += rows;
       }
     }
-    int4 tot;
-    const int4 ex = block_excl_scan4(cnt, scan_tmp, tot);
-    int hpos = ex.x, hrow = ex.y, lpos = tot.x + ex.z, lrow = tot.y + ex.w;
+    int4 inc = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int4 y = make_int4(__shfl_up_sync(0xffffffffu, inc.x, o), __shfl_up_sync(0xffffffffu, inc.y, o),
+                               __shfl_up_sync(0xffffffffu, inc.z, o), __shfl_up_sync(0xffffffffu, inc.w, o));
+      if (lane >= o) {
+        inc.x += y.x;
+        inc.y += y.y;
+        inc.z += y.z;
+        inc.w += y.w;
+      }
+    }
+    const int4 tot = make_int4(__shfl_sync(0xffffffffu, inc.x, 31), __shfl_sync(0xffffffffu, inc.y, 31),
+                               __shfl_sync(0xffffffffu, inc.z, 31), __shfl_sync(0xffffffffu, inc.w, 31));
+    int hpos = inc.x - cnt.x, hrow = inc.y - cnt.y;
+    int lpos = tot.x + inc.z - cnt.z, lrow = tot.y + inc.w - cnt.w;
     for (int b = lo; b < hi; ++b) {
-      int nd;
-      const int kind = classify(b, nd);
+      const int4 r = req[b];
+      const int kind = r.x, nd = r.y;
       int pos, rows = 0;
       if (kind == KIND_SOFTMAX) {
         rows = 2 * nd + 1;
@@ -121,11 +145,11 @@ struct ChainProblem {
         lrow += rows;
       }
       tab.info[pos] = make_info(b, kind < 0 ? 0 : kind, nd < 0 ? 0 : min(nd, 0x7ff));
-      const Scale2 c = scale_for(temperature[b]);
+      const Scale2 c = scale_for(__int_as_float(r.z));
       tab.scale[pos] = make_float2(c.hi, c.lo);
       if (kind < 0 && blockIdx.x == 0) write_failed(b, 0x20);
     }
-    if (threadIdx.x == 0) {
+    if (lane == 0) {
       tab.rstart[n_req] = tot.y + tot.w;
       sh.n_pos = n_req;
       sh.n_draw_cap = tot.x;

@@ -118,6 +118,10 @@ __device__ __forceinline__ void bulk_copy_g2s_hint(void* smem_dst, const void* g
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
+// L2 prefetch of the line holding p (a hint: no value is read).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 __device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

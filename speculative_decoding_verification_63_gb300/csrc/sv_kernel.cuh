@@ -48,7 +48,9 @@
 //   static constexpr int kAuxBytes       per-position aux table (0, 8, 16)
 //   static constexpr bool kWarpFinalize  finalizes run per warp (else group)
 //   static constexpr bool kHasDraws      the problem publishes draw passes
-//   void preamble(Shared&, PosTables&, int4* scan_tmp) const   (all threads)
+//   void prefetch_args(int lane) const  L2 hints issued before the dependency wait
+//   void preamble(Shared&, PosTables&, int4* scan_tmp, unsigned char* scratch) const
+//        (all threads; scratch: the chunk ring, free until the preamble ends)
 //   void fill_stage(const PosTables&, int row_local, StageMeta&, ResMeta&)
 //        -> a main-pass chunk: kind, scale, source, ticket fields (producer)
 //   void fill_resid(const P2Job&, int chunk, StageMeta&, ResMeta&) const
@@ -692,6 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const P prob) {
   // work on the stream (which may have produced the inputs, and used the
   // same workspace) before touching global memory, and let the next launch
   // start filling SMs as this one drains.
+  if (threadIdx.x < 32) prob.prefetch_args(threadIdx.x);
   grid_dependency_wait();
   grid_launch_dependents();
   // 128-byte aligned base (the launch adds 128 bytes of slack)
@@ -728,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const P prob) {
     sh.fin_cmd = -1;
     sh.n_draw_cap = 0;
   }
-  prob.preamble(sh, tab, scan_tmp);
+  prob.preamble(sh, tab, scan_tmp, stages);
   __syncthreads();
 
   if (P::kCtrl && blockIdx.x >= gridDim.x - n_ctrl_of(prob)) {

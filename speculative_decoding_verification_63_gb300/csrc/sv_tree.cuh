@@ -92,7 +92,9 @@ struct TreeProblem {
     record_error(&ws.hdr->error, flag);
   }
 
-  __device__ void preamble(Shared& sh, PosTables& tab, int4* scan_tmp) const {
+  __device__ void prefetch_args(int) const {}
+
+  __device__ void preamble(Shared& sh, PosTables& tab, int4* scan_tmp, unsigned char*) const {
     const int per = (n_req + kThreads - 1) / kThreads;
     const int lo = min(static_cast<int>(threadIdx.x) * per, n_req);
     const int hi = min(lo + per, n_req);
