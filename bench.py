@@ -52,8 +52,10 @@ FALLBACK_HBM_GBS = 6800.0
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 20000 launches; reference arm: 256 rounds)")
+    ap.add_argument("--warmup", type=int, default=None,
+                    help="untimed steps (default: 50; reference arm: 3)")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--kernel-only", action="store_true",
                     help="profiling runs: eager launches only (no graphs, no end-to-end leg, "
@@ -243,22 +245,40 @@ def time_oracle(inp, budget_s: float, max_steps: int | None = None):
 
 
 def run_reference(args, dist):
+    """The reference arm: the fp64 CPU oracle, as it stands, on one host
+    core.  One step is one request round of the headline batch (requests
+    taken in order, so greedy and sampled rounds alternate as in the batch);
+    W untimed steps, then exactly K timed ones.  Without --steps/--warmup
+    the arm runs 256 timed rounds after 3 warm-up rounds (a few seconds)."""
     if dist.rank != 0:
         return 0
+    import oracle
+    lib = oracle.load()
     inp = _make_set(0)
     B = inp["B"]
-    # each step is one full verification of the batch on one host core; the
-    # run is bounded to about a minute whatever --steps asks for
-    probe_steps, probe_s = time_oracle(inp, 0.0, max_steps=1)
-    per_step = probe_s
-    steps = max(1, min(args.steps, int(60.0 / max(per_step, 1e-9))))
-    n, el = time_oracle(inp, 0.0, max_steps=steps)
-    value = B * n / el
-    sample = f"{n} full steps of the headline batch ({n * B} request rounds), fp64 C, 1 thread"
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": n,
-            "requested_steps": args.steps, "warmup": 1, "ms_per_step": el / n * 1e3,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": config_dict(inp), "impl": "reference",
+    keys = ("target", "draft", "tokens", "temperature", "uniforms", "num_drafts", "top_k")
+    rounds = [{k: inp[k][b:b + 1] for k in keys} for b in range(B)]  # views, no copies
+
+    def step(i):
+        r = rounds[i % B]
+        oracle.verify_chain(r["target"], r["draft"], r["tokens"], r["temperature"],
+                            r["uniforms"], num_drafts=r["num_drafts"], top_k=r["top_k"], lib=lib)
+
+    K = args.steps if args.steps is not None else 256
+    W = max(args.warmup if args.warmup is not None else 3, 3)
+    for i in range(W):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(K):
+        step(W + i)
+    el = time.perf_counter() - t0
+    value = K / el
+    sample = (f"{K} request rounds of the headline batch, one per step, requests in batch "
+              "order (half greedy, half sampled), fp64 C, one host thread")
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": K,
+            "warmup": W, "ms_per_step": el / K * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(inp), "impl": "reference",
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -474,6 +494,8 @@ def main():
         dist.init(device_ok=False)
         rc = run_reference(args, dist)
     else:
+        args.steps = 20000 if args.steps is None else args.steps
+        args.warmup = 50 if args.warmup is None else args.warmup
         dist.init(device_ok=True)
         rc = run_ours(args, dist)
     dist.close()
