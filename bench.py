@@ -115,12 +115,15 @@ CHAIN_KERNEL_SOURCES = ("sv_device.cuh", "sv_rowpass.cuh", "sv_kernel.cuh", "sv_
 
 def source_hash() -> str:
     """Hash of the chain kernel's CUDA sources, to tell whether a stored ncu
-    figure is current."""
+    figure is current.  Comments and blank lines are left out, so editing a
+    comment keeps the figure; any change to the code drops it."""
+    import re
     d = os.path.join(ROOT, "speculative_decoding_verification_63_gb300", "csrc")
     h = hashlib.sha256()
     for name in CHAIN_KERNEL_SOURCES:
-        with open(os.path.join(d, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        with open(os.path.join(d, name)) as f:
+            code = [re.sub(r"//.*", "", line).rstrip() for line in f]
+        h.update(name.encode() + b"\0" + "\n".join(l for l in code if l).encode())
     return h.hexdigest()[:16]
 
 

@@ -10,20 +10,22 @@
 //
 // Inside the persistent kernel (sv_kernel.cuh):
 //   main pass   every row the step reads is reduced chunk by chunk to
-//               (max, sum exp) or (max, lowest argmax);
-//   request     when a request's last chunk is booked, one finalizer warp
-//   finalize    merges its rows, runs the accept tests and the
-//               prefix-terminating scan, writes the accepted prefix; a
-//               greedy request is then complete, a sampled one publishes
-//               its draw (row pair n) in the global draw list;
-//   draw pass   claims beyond the main pass stream the published row pairs
-//               again as draw chunks (16 KB of p_n | 16 KB of q_n), spread
-//               over all CTAs; each consumer warp turns its 256-token
-//               segments into residual weights and their sums;
-//   draw        when the draw's last chunk is booked, one finalizer warp
-//   finalize    takes the fp64 prefix over the segment sums, finds the
-//               segment holding u * S, rescans it with bit-identical
-//               arithmetic and writes the emitted token.
+//               (max, sum exp) or (max, lowest argmax), one 64-bit partial
+//               per chunk, on the streaming CTAs;
+//   request     a warp of a control CTA polls the request's partials as
+//   finalize    they are written, merges its rows, runs the accept tests
+//               and the prefix-terminating scan; a greedy request is then
+//               complete, a sampled one publishes its draw (row pair n) as
+//               a self-marking record, then writes the accepted prefix;
+//   draw pass   the streaming CTAs' scouts, each walking its static share
+//               of the draw claims, stream the published row pairs again
+//               as draw chunks (16 KB of p_n | 16 KB of q_n); each consumer
+//               warp turns its 256-token segments into residual weights and
+//               their sums;
+//   draw        the same control warp polls the draw's segment sums, takes
+//   finalize    the float-pair prefix over them, finds the segment holding
+//               u * S, rescans it with bit-identical arithmetic and writes
+//               the emitted token.
 #pragma once
 
 #include "sv_kernel.cuh"
