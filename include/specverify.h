@@ -30,9 +30,10 @@
  *     checks and launch errors only; errors found while the kernel reads the
  *     data are recorded in the workspace and read with sv_get_error().
  *   - A workspace must be zeroed once with sv_workspace_init() before its
- *     first use.  Every call leaves its counters zeroed again, whatever the
- *     sizes, so one workspace (large enough for each call) serves chain and
- *     tree calls of any shape in sequence; after a device error it must be
+ *     first use.  Every call leaves each word it wrote zeroed again (the
+ *     role that reads a word last clears it), whatever the sizes, so one
+ *     workspace (large enough for each call) serves chain and tree calls of
+ *     any shape in sequence; after a device error it must be
  *     re-initialised.  One workspace serves one call at a time: calls that
  *     may overlap on the GPU need separate workspaces.
  *   - Status codes are never negative.
