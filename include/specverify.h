@@ -249,20 +249,25 @@ sv_status sv_tree_mask(const sv_tree_mask_args* args, void* workspace, size_t ws
  * E[N] = (1 - a^(K+1)) / (1 - a) when every alpha_i = a).  The inputs an
  * adaptive draft length or an on/off switch for speculation would use.
  *
- * Reads the target, draft, num_drafts, temperature and top_k fields of a
- * chain call's arguments (B, K, V, dtype and strides as there; tokens,
- * uniforms and the outputs are not used and may be NULL).  Outputs:
+ * Reads the target, draft, num_drafts, temperature, top_k and max_top_k
+ * fields of a chain call's arguments (B, K, V, dtype and strides as there;
+ * tokens, uniforms and the outputs are not used and may be NULL).  Outputs:
  *   alpha [B][K]: alpha_i for i < num_drafts[b], NaN beyond.  Greedy
  *     requests (t == 0) have one-hot p and q: alpha_i = 1 iff argmax p_i ==
- *     argmax q_i (lowest id on ties), else 0.
+ *     argmax q_i (lowest id on ties), else 0.  With a top-k filter p_i and
+ *     q_i are each restricted to their own top-k set ([N02] sec. 5.4), so
+ *     alpha_i sums min(p_i, q_i) over the tokens both sets hold.
  *   expected [B]: sum_{j=0..nd} prod_{i<j} alpha_i, the expected number of
  *     tokens the round emits under these rates.
- * A request with top-k filtering (0 < top_k < V) is not supported here and
- * is reported as SV_DERR_ARG, like a bad num_drafts or temperature; NaN or
- * +inf logits give SV_DERR_NONFINITE, a row without mass SV_DERR_MASS.
- * The failing request gets NaN.  The workspace: one sized by
- * sv_chain_workspace_bytes (its header and per-request counters are used
- * and left zeroed).
+ * With a top_k array and max_top_k > 0 the call first runs the chain's
+ * top-k pass (the same lists sv_verify_chain builds) and needs a workspace
+ * of sv_chain_workspace_bytes(B, K, V, dtype, max_top_k) bytes; a filter
+ * above max_top_k, or any filter when max_top_k is 0, is reported as
+ * SV_DERR_ARG, like a bad num_drafts or temperature.  NaN or +inf logits
+ * give SV_DERR_NONFINITE, a row without mass SV_DERR_MASS.  The failing
+ * request gets NaN.  Without top-k lists the workspace only needs its
+ * header and per-request counters (any sv_chain_workspace_bytes size); what
+ * the call uses is left zeroed.
  */
 sv_status sv_row_stats(const sv_chain_args* args, float* alpha, float* expected,
                        void* workspace, size_t ws_bytes, sv_stream_t stream);
@@ -288,10 +293,11 @@ sv_status sv_selftest_wait_timeout(void* workspace, size_t ws_bytes,
  * SV_NOALLOC_SCRATCH_BYTES long, reserved when the library's module loads;
  * the calls themselves allocate nothing.
  *
- *   - The first call on a device (with that device current) looks up the
- *     array's address (cudaGetSymbolAddress) and zeroes it on `stream`
- *     (cudaMemsetAsync), ahead of the kernel; make that first call before
- *     any stream capture that should contain only the verification.
+ *   - Every call looks up the array's address on the current device
+ *     (cudaGetSymbolAddress).  The first call in a context (after a device
+ *     reset too) zeroes it on `stream` (cudaMemsetAsync), ahead of the
+ *     kernel; make that first call before any stream capture that should
+ *     contain only the verification.
  *   - A call whose sv_chain_workspace_bytes(...) exceeds
  *     SV_NOALLOC_SCRATCH_BYTES is rejected with SV_EWORKSPACE before any
  *     device work; use sv_verify_chain with a caller workspace instead.

@@ -32,6 +32,13 @@ LIBRARY = os.path.join(_HERE, "libsv_oracle.so")
 # oracle status codes (mirror the #defines in sv_oracle.c)
 OK, ENONFINITE, ETOKEN, EMASS, ETREE, EARG = 0, 1, 2, 3, 4, 5
 
+# Relative distance from a decision boundary below which a decision is
+# "near": an accept test with |u q - p| / q < NEAR, or an inverse-CDF draw
+# whose u S lies within NEAR S of a CDF step.  For such draws the batch
+# functions also report the range of tokens a target perturbed by up to
+# NEAR S can give (draw_lo .. draw_hi).
+NEAR = 1e-6
+
 _lock = threading.Lock()
 _lib = None
 
@@ -71,9 +78,13 @@ def _declare(lib):
     lib.svo_residual.restype = ctypes.c_double
     lib.svo_icdf.argtypes = [_P, ctypes.c_int, ctypes.c_double, _P]
     lib.svo_icdf.restype = ctypes.c_int
-    lib.svo_verify_chain.argtypes = [ctypes.c_int] * 4 + [_P] * 7 + [_P] * 8
+    lib.svo_icdf_window.argtypes = [_P, ctypes.c_int, ctypes.c_double, ctypes.c_double, _P, _P]
+    lib.svo_icdf_window.restype = ctypes.c_int
+    lib.svo_verify_chain.argtypes = ([ctypes.c_int] * 4 + [_P] * 7 + [_P] * 8 +
+                                     [ctypes.c_double, _P, _P])
     lib.svo_verify_chain.restype = ctypes.c_int
-    lib.svo_verify_tree.argtypes = [ctypes.c_int] * 7 + [_P] * 10 + [_P] * 7
+    lib.svo_verify_tree.argtypes = ([ctypes.c_int] * 7 + [_P] * 10 + [_P] * 7 +
+                                    [ctypes.c_double, _P, _P, _P])
     lib.svo_verify_tree.restype = ctypes.c_int
     lib.svo_tree_mask.argtypes = [ctypes.c_int] * 3 + [_P] * 5
     lib.svo_tree_mask.restype = ctypes.c_int
@@ -133,10 +144,22 @@ def icdf(w, u: float, lib=None):
     return t, float(m[0])
 
 
+def icdf_window(w, u: float, radius: float, lib=None):
+    """(lo, hi, count): the ids of the first and last positive-weight token
+    whose CDF step meets [u S - radius S, u S + radius S], and how many
+    positive-weight tokens lie between them (see svo_icdf_window)."""
+    lib = lib or load()
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    lo = np.zeros(1, dtype=np.int32)
+    hi = np.zeros(1, dtype=np.int32)
+    n = lib.svo_icdf_window(_ptr(w), w.shape[0], float(u), float(radius), _ptr(lo), _ptr(hi))
+    return int(lo[0]), int(hi[0]), int(n)
+
+
 # ------------------------------------------------------------------- chain
 
 def verify_chain(target, draft, tokens, temperature, uniforms,
-                 num_drafts=None, top_k=None, lib=None) -> dict:
+                 num_drafts=None, top_k=None, lib=None, near: float = NEAR) -> dict:
     """Chain verification of a batch (see svo_verify_chain in sv_oracle.c).
 
     target [B][K+1][V], draft [B][K][V] (uint16 bf16 bits or float32),
@@ -158,14 +181,17 @@ def verify_chain(target, draft, tokens, temperature, uniforms,
     out = dict(out_tokens=np.zeros((B, K + 1), np.int32), out_len=np.zeros(B, np.int32),
                accept_len=np.zeros(B, np.int32), p_at=np.zeros((B, K)),
                q_at=np.zeros((B, K)), margin_accept=np.zeros(B), margin_draw=np.zeros(B),
-               status=np.zeros(B, np.int32))
+               status=np.zeros(B, np.int32), draw_lo=np.zeros(B, np.int32),
+               draw_hi=np.zeros(B, np.int32))
     lib.svo_verify_chain(B, K, V, dt, _ptr(target), _ptr(draft), _ptr(tokens), _ptr(nd),
                          _ptr(temperature), _ptr(tk), _ptr(uniforms),
                          _ptr(out["out_tokens"]), _ptr(out["out_len"]),
                          _ptr(out["accept_len"]), _ptr(out["p_at"]), _ptr(out["q_at"]),
                          _ptr(out["margin_accept"]), _ptr(out["margin_draw"]),
-                         _ptr(out["status"]))
+                         _ptr(out["status"]), float(near), _ptr(out["draw_lo"]),
+                         _ptr(out["draw_hi"]))
     out["margin"] = np.minimum(out["margin_accept"], out["margin_draw"])
+    out["margin_walk"] = np.full(B, np.inf)
     return out
 
 
@@ -186,7 +212,7 @@ TREE_MODES = {"mss": 0, "noreplace": 1, "naive": 2}
 
 def verify_tree(target, draft, node_tokens, parent, q_row, temperature,
                 u_accept, u_sample, num_nodes=None, top_k=None, max_depth=None,
-                mode: str = "mss", lib=None) -> dict:
+                mode: str = "mss", lib=None, near: float = NEAR) -> dict:
     """Token-tree verification (VerifyGreedy, and MSS, MSS without
     replacement or naive sampling by `mode`), see svo_verify_tree."""
     lib = lib or load()
@@ -208,7 +234,8 @@ def verify_tree(target, draft, node_tokens, parent, q_row, temperature,
                out_len=np.zeros(B, np.int32), accept_len=np.zeros(B, np.int32),
                accepted_nodes=np.zeros((B, max(max_depth, 1)), np.int32),
                margin_accept=np.zeros(B), margin_draw=np.zeros(B),
-               status=np.zeros(B, np.int32))
+               status=np.zeros(B, np.int32), margin_walk=np.zeros(B),
+               draw_lo=np.zeros(B, np.int32), draw_hi=np.zeros(B, np.int32))
     lib.svo_verify_tree(B, N, M, V, dt, max_depth, TREE_MODES[mode], _ptr(target),
                         _ptr(draft),
                         _ptr(node_tokens), _ptr(parent), _ptr(q_row), _ptr(nn),
@@ -216,7 +243,8 @@ def verify_tree(target, draft, node_tokens, parent, q_row, temperature,
                         _ptr(out["out_tokens"]), _ptr(out["out_len"]),
                         _ptr(out["accept_len"]), _ptr(out["accepted_nodes"]),
                         _ptr(out["margin_accept"]), _ptr(out["margin_draw"]),
-                        _ptr(out["status"]))
+                        _ptr(out["status"]), float(near), _ptr(out["margin_walk"]),
+                        _ptr(out["draw_lo"]), _ptr(out["draw_hi"]))
     out["margin"] = np.minimum(out["margin_accept"], out["margin_draw"])
     if max_depth == 0:
         out["accepted_nodes"] = out["accepted_nodes"][:, :0]

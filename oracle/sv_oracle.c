@@ -209,6 +209,45 @@ int svo_icdf(const double* w, int V, double u, double* margin) {
   return last;
 }
 
+/*
+ * The tokens an inverse-CDF draw can give when its target u*S is known only
+ * to within radius*S: every t with w(t) > 0 whose step [C(t-1), C(t)) meets
+ * [u*S - radius*S, u*S + radius*S] (C and S summed in ascending id order as
+ * in svo_icdf).  *lo and *hi receive the smallest and largest such id; they
+ * are equal to the svo_icdf token when no other step is that close.  With
+ * radius 0 the range is the svo_icdf token alone.  Returns the number of
+ * positive-weight tokens in [*lo, *hi], or -1 (and *lo = *hi = -1) when S is
+ * not positive.  The parity tests use it to bound a draw whose uniform lies
+ * within the kernel's rounding of a CDF step.
+ */
+int svo_icdf_window(const double* w, int V, double u, double radius, int* lo, int* hi) {
+  double S = 0.0;
+  for (int t = 0; t < V; ++t) S += w[t];
+  *lo = -1;
+  *hi = -1;
+  if (!(S > 0.0)) return -1;
+  const double a = (u - radius) * S, b = (u + radius) * S;
+  double c_prev = 0.0, c = 0.0;
+  int count = 0;
+  for (int t = 0; t < V; ++t) {
+    c_prev = c;
+    c += w[t];
+    if (!(w[t] > 0.0)) continue;
+    if (c > a && c_prev <= b) {
+      if (*lo < 0) *lo = t;
+      *hi = t;
+    }
+  }
+  /* rounding can leave u*S at or beyond the last step: svo_icdf then takes
+     the last positive weight, which the window must hold too */
+  if (*lo < 0) {
+    for (int t = 0; t < V; ++t)
+      if (w[t] > 0.0) *lo = *hi = t;
+  }
+  for (int t = *lo; t >= 0 && t <= *hi; ++t) count += w[t] > 0.0;
+  return count;
+}
+
 /* relative distance of an accept test  u*q < p  from its boundary */
 static double accept_margin(double u, double q, double p) {
   if (!(q > 0.0)) return INFINITY; /* u*0 < p is decided by p > 0 alone */
@@ -232,6 +271,9 @@ static double accept_margin(double u, double q, double p) {
  * margin_accept [B] = smallest relative distance |u q - p| / q of an accept
  * test taken to its boundary, margin_draw [B] = the inverse-CDF margin of the
  * final draw (+inf where the decisions are exact, e.g. greedy), status [B].
+ * draw_lo, draw_hi [B] (may be NULL): the emitted token's id, or, when the
+ * final draw's margin is below `near`, the id range svo_icdf_window gives
+ * for radius `near` on the same weights (-1 for a failed request).
  */
 int svo_verify_chain(int B, int K, int V, int dtype, const void* target,
                      const void* draft, const int* tokens,
@@ -239,7 +281,7 @@ int svo_verify_chain(int B, int K, int V, int dtype, const void* target,
                      const int* top_k, const float* uniforms, int* out_tokens,
                      int* out_len, int* accept_len, double* p_at,
                      double* q_at, double* margin_accept, double* margin_draw,
-                     int* status) {
+                     int* status, double near, int* draw_lo, int* draw_hi) {
   const size_t es = dtype == 0 ? 2 : 4;
   double* p = (double*)malloc(sizeof(double) * (size_t)V);
   double* q = (double*)malloc(sizeof(double) * (size_t)V);
@@ -265,6 +307,7 @@ int svo_verify_chain(int B, int K, int V, int dtype, const void* target,
     margin_accept[b] = INFINITY;
     margin_draw[b] = INFINITY;
     status[b] = SVO_OK;
+    if (draw_lo) draw_lo[b] = draw_hi[b] = -1;
 
     int st = SVO_OK;
     if (nd < 0 || nd > K || !(T >= 0.0)) st = SVO_EARG;
@@ -316,10 +359,14 @@ int svo_verify_chain(int B, int K, int V, int dtype, const void* target,
             double S = svo_residual(p, q, V, w);
             token = S > 0.0 ? svo_icdf(w, V, (double)u[K], &mg)
                             : svo_icdf(p, V, (double)u[K], &mg);
+            if (draw_lo && mg < near)
+              svo_icdf_window(S > 0.0 ? w : p, V, (double)u[K], near, &draw_lo[b], &draw_hi[b]);
           }
         } else if (st == SVO_OK) {
           /* all drafts accepted: bonus token from p_{nd+1} */
           token = svo_icdf(p, V, (double)u[K], &mg);
+          if (draw_lo && mg < near)
+            svo_icdf_window(p, V, (double)u[K], near, &draw_lo[b], &draw_hi[b]);
         }
         margin_draw[b] = mg;
         if (st == SVO_OK && token < 0) st = SVO_EMASS;
@@ -330,6 +377,7 @@ int svo_verify_chain(int B, int K, int V, int dtype, const void* target,
     out[n] = token;
     out_len[b] = n + 1;
     accept_len[b] = n;
+    if (draw_lo && !(margin_draw[b] < near)) draw_lo[b] = draw_hi[b] = token;
   }
   free(p);
   free(q);
@@ -377,7 +425,10 @@ int svo_verify_chain(int B, int K, int V, int dtype, const void* target,
  *
  * Outputs: out_tokens [B][max_depth+1], accepted_nodes [B][max_depth]
  * (-1 padded), out_len, accept_len, margin_accept, margin_draw, status as
- * for the chain.
+ * for the chain.  margin_walk [B] (may be NULL): the smallest margin of the
+ * draws that chose a child (naive mode; +inf otherwise), i.e. of the draws
+ * that decide the path as the accept tests do in MSS.  draw_lo, draw_hi [B]
+ * (may be NULL): as for the chain, for the draw of the emitted token.
  */
 #define SVO_TREE_MSS 0
 #define SVO_TREE_NOREPLACE 1
@@ -391,7 +442,8 @@ int svo_verify_tree(int B, int N, int M, int V, int dtype, int max_depth, int mo
                     const float* u_accept, const float* u_sample,
                     int* out_tokens, int* out_len, int* accept_len,
                     int* accepted_nodes, double* margin_accept,
-                    double* margin_draw, int* status) {
+                    double* margin_draw, int* status, double near,
+                    double* margin_walk, int* draw_lo, int* draw_hi) {
   const size_t es = dtype == 0 ? 2 : 4;
   double* p = (double*)malloc(sizeof(double) * (size_t)V);
   double* r = (double*)malloc(sizeof(double) * (size_t)V);
@@ -419,6 +471,10 @@ int svo_verify_tree(int B, int N, int M, int V, int dtype, int max_depth, int mo
     margin_accept[b] = INFINITY;
     margin_draw[b] = INFINITY;
     status[b] = SVO_OK;
+    if (margin_walk) margin_walk[b] = INFINITY;
+    if (draw_lo) draw_lo[b] = draw_hi[b] = -1;
+    const double* wfinal = NULL; /* weights of the final draw */
+    double ufinal = 0.0, mfinal = INFINITY;
 
     int st = SVO_OK;
     if (nn < 1 || nn > N || !(T >= 0.0) || mode < 0 || mode > 2) st = SVO_EARG;
@@ -460,7 +516,14 @@ int svo_verify_tree(int B, int N, int M, int V, int dtype, int max_depth, int mo
         int next = -1;
         for (int c = node + 1; c < nn; ++c)
           if (par[c] == node && tok[c] == x) { next = c; break; }
-        if (next < 0) { token = x; break; }
+        if (next < 0) {
+          token = x;
+          wfinal = p;
+          ufinal = (double)ua[node];
+          mfinal = mgn;
+          break;
+        }
+        if (margin_walk && mgn < margin_walk[b]) margin_walk[b] = mgn;
         out[L] = x;
         acc[L] = next;
         ++L;
@@ -474,6 +537,9 @@ int svo_verify_tree(int B, int N, int M, int V, int dtype, int max_depth, int mo
       if (!has_child) { /* leaf: bonus token from p_node */
         token = svo_icdf(p, V, (double)u_sample[b], &mg);
         margin_draw[b] = mg;
+        wfinal = p;
+        ufinal = (double)u_sample[b];
+        mfinal = mg;
         break;
       }
       memcpy(r, p, sizeof(double) * (size_t)V);
@@ -509,6 +575,9 @@ int svo_verify_tree(int B, int N, int M, int V, int dtype, int max_depth, int mo
       }
       token = svo_icdf(r, V, (double)u_sample[b], &mg);
       margin_draw[b] = mg;
+      wfinal = r;
+      ufinal = (double)u_sample[b];
+      mfinal = mg;
       break;
     }
     if (st == SVO_OK && token < 0) st = SVO_EMASS;
@@ -522,6 +591,10 @@ int svo_verify_tree(int B, int N, int M, int V, int dtype, int max_depth, int mo
     out[L] = token;
     out_len[b] = L + 1;
     accept_len[b] = L;
+    if (draw_lo) {
+      draw_lo[b] = draw_hi[b] = token;
+      if (wfinal && mfinal < near) svo_icdf_window(wfinal, V, ufinal, near, &draw_lo[b], &draw_hi[b]);
+    }
   }
   free(p);
   free(r);

@@ -133,19 +133,22 @@ def tree_mask(parent, num_nodes=None, words: int | None = None,
 
 
 def row_stats(target_logits, draft_logits, temperature, num_drafts=None, top_k=None,
-              ws: torch.Tensor | None = None) -> dict:
-    """Per-position acceptance rates alpha [B][K] (sum min(p_i, q_i)) and
-    the expected tokens per round [B] of a chain batch (device tensors)."""
+              ws: torch.Tensor | None = None, max_top_k: int | None = None) -> dict:
+    """Per-position acceptance rates alpha [B][K] (sum min(p_i, q_i), over
+    the top-k sets of filtered requests) and the expected tokens per round
+    [B] of a chain batch (device tensors)."""
     B, K1, V = target_logits.shape
     K = K1 - 1
     dev = target_logits.device
+    if max_top_k is None:
+        max_top_k = 0 if top_k is None else SV_MAX_TOPK
     out = dict(alpha=torch.empty((B, K), dtype=torch.float32, device=dev),
                expected=torch.empty(B, dtype=torch.float32, device=dev))
     if ws is None:
-        ws = workspace(sv_chain_workspace_bytes(max(B, 1), K, V, dtype_code(target_logits)),
-                       dev, "chain")
+        ws = workspace(sv_chain_workspace_bytes(max(B, 1), K, V, dtype_code(target_logits),
+                                                max_top_k), dev, "chain")
     sv_row_stats(target_logits, draft_logits, temperature, out["alpha"], out["expected"], ws,
-                 num_drafts=num_drafts, top_k=top_k)
+                 num_drafts=num_drafts, top_k=top_k, max_top_k=max_top_k)
     return out
 
 

@@ -370,7 +370,7 @@ def sv_tree_mask(parent, mask, depth, workspace, num_nodes=None, stream=None) ->
 
 
 def sv_row_stats(target_logits, draft_logits, temperature, alpha, expected, workspace,
-                 num_drafts=None, top_k=None, stream=None) -> None:
+                 num_drafts=None, top_k=None, max_top_k: int = 0, stream=None) -> None:
     """Enqueue sv_row_stats: alpha [B][K] = sum min(p_i, q_i) per position
     and expected [B] tokens per round."""
     B, K1, V = target_logits.shape
@@ -392,6 +392,7 @@ def sv_row_stats(target_logits, draft_logits, temperature, alpha, expected, work
     _check(alpha, torch.float32, (B, K), "alpha")
     _check(expected, torch.float32, (B,), "expected")
     a.temperature, a.num_drafts, a.top_k = _ptr(temperature), _ptr(num_drafts), _ptr(top_k)
+    a.max_top_k = max_top_k
     st = lib().sv_row_stats(ctypes.byref(a), _ptr(alpha), _ptr(expected), _ptr(workspace),
                             workspace.numel() * workspace.element_size(), _stream(stream))
     if st != SV_OK:

@@ -1,5 +1,6 @@
 // specverify.cu -- C ABI of libspecverify (see include/specverify.h):
 // argument checks, workspace layout, launch of the sm_103a kernels.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -199,6 +200,42 @@ sv_status launch_topk(const TopkPass& t, int grid, cudaStream_t stream) {
   return e == cudaSuccess ? SV_OK : SV_ECUDA;
 }
 
+// The top-k pass of a chain call's filtered requests: every filtered row
+// reduced to its top-k (logit, id) list and (m, Z) in the workspace's
+// scratch region (layout TL).
+sv_status run_topk_pass(const sv_chain_args* a, void* workspace, const Layout& L,
+                        const TopkLayout& TL, const DeviceInfo& dev, cudaStream_t st) {
+  const int es = es_of(a->dtype);
+  char* scratch = static_cast<char*>(workspace) + L.scratch;
+  TopkPass t;
+  t.n_req = a->B;
+  t.K = a->K;
+  t.V = a->V;
+  t.es = es;
+  t.max_topk = a->max_top_k;
+  t.n_seg = TL.n_seg;
+  t.seg_len = TL.seg_len;
+  t.has_draft = a->draft_logits != nullptr;
+  t.target = static_cast<const char*>(a->target_logits);
+  t.t_stride = a->target_row_stride * es;
+  t.draft = static_cast<const char*>(a->draft_logits);
+  t.d_stride = a->draft_logits ? a->draft_row_stride * es : 0;
+  t.vec = aligned16(a->target_logits, t.t_stride) &&
+          (a->draft_logits == nullptr || aligned16(a->draft_logits, t.d_stride));
+  t.num_drafts = a->num_drafts;
+  t.temperature = a->temperature;
+  t.top_k = a->top_k;
+  t.seg_lists = reinterpret_cast<float2*>(scratch + TL.seg_lists);
+  t.seg_count = reinterpret_cast<int*>(scratch + TL.seg_count);
+  t.lists = reinterpret_cast<float2*>(scratch + TL.lists);
+  t.mz = reinterpret_cast<float2*>(scratch + TL.mz);
+  t.row_done = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + L.topk_done);
+  const int64_t items = static_cast<int64_t>(a->B) * (2 * a->K + 1) * TL.n_seg;
+  const int64_t ctas = std::min<int64_t>((items + kTkWarps - 1) / kTkWarps,
+                                         static_cast<int64_t>(kTkCtasPerSm) * dev.sms);
+  return launch_topk(t, static_cast<int>(ctas), st);
+}
+
 __global__ void wait_selftest_kernel(WsHeader* hdr, uint64_t limit_ns) {
   __shared__ uint64_t bar;
   if (threadIdx.x == 0) {
@@ -219,32 +256,74 @@ __global__ void wait_selftest_kernel(WsHeader* hdr, uint64_t limit_ns) {
 // Callers that cannot pass a workspace -- no device allocator at hand where
 // they call, or a call site where allocating device memory is not allowed or
 // could block -- get this per-device array instead.  It is reserved when the
-// module loads; the entry point below only looks up its address once per
-// device and never allocates.
+// module loads; the entry point below only looks up its address and never
+// allocates.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SV_NOALLOC_SCRATCH_BYTES];
 
 namespace {
 
+// What the library knows about the scratch of one device: the context it
+// was zeroed in (and its address there).  After a device reset or a new
+// primary context the module is loaded again; the array is then looked up
+// and zeroed again before its first use, so no stale address is ever used.
 struct NoallocSlot {
+  unsigned long long ctx_id = 0;
   void* ptr = nullptr;
+  bool zeroed = false;
 };
 NoallocSlot g_noalloc[64];
 
-// The scratch of the current device; the first call for a device looks up
-// its address and zeroes it on `stream` (ahead of whatever follows there).
+// The driver's unique id of the current context (0 when it cannot be read):
+// cuCtxGetCurrent and cuCtxGetId, resolved through the runtime, so the
+// library needs no link against the driver library.
+unsigned long long current_ctx_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static bool resolved = false;
+  if (!resolved) {  // under g_mu
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) ==
+            cudaSuccess &&
+        q1 == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) ==
+            cudaSuccess &&
+        q2 == cudaDriverEntryPointSuccess) {
+      get_current = reinterpret_cast<GetCurrent>(f1);
+      get_id = reinterpret_cast<GetId>(f2);
+    }
+    resolved = true;
+  }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// The scratch of the current device.  Its address is looked up on every
+// call (cudaGetSymbolAddress allocates nothing); the first call in a
+// context zeroes it on `stream`, ahead of whatever follows there.
 sv_status noalloc_scratch(cudaStream_t stream, void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SV_ECUDA;
   if (dev < 0 || dev >= 64) return SV_EUNSUPPORTED;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return SV_ECUDA;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (g_noalloc[dev].ptr == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-      return SV_ECUDA;
+  const unsigned long long id = current_ctx_id();
+  NoallocSlot& sl = g_noalloc[dev];
+  if (!sl.zeroed || sl.ctx_id != id || sl.ptr != p) {
     if (cudaMemsetAsync(p, 0, SV_NOALLOC_SCRATCH_BYTES, stream) != cudaSuccess) return SV_ECUDA;
-    g_noalloc[dev].ptr = p;
+    sl.zeroed = true;
+    sl.ctx_id = id;
+    sl.ptr = p;
   }
-  *out = g_noalloc[dev].ptr;
+  *out = p;
   return SV_OK;
 }
 
@@ -357,33 +436,7 @@ sv_status sv_verify_chain(const sv_chain_args* a, void* workspace, size_t ws_byt
   if (a->top_k != nullptr && a->max_top_k > 0) {
     // the top-k lists first; the persistent kernel finalizes top-k
     // requests from them
-    TopkPass t;
-    t.n_req = a->B;
-    t.K = a->K;
-    t.V = a->V;
-    t.es = es;
-    t.max_topk = a->max_top_k;
-    t.n_seg = TL.n_seg;
-    t.seg_len = TL.seg_len;
-    t.has_draft = a->draft_logits != nullptr;
-    t.target = p.target;
-    t.t_stride = p.t_stride;
-    t.draft = p.draft;
-    t.d_stride = p.d_stride;
-    t.vec = aligned16(a->target_logits, p.t_stride) &&
-            (a->draft_logits == nullptr || aligned16(a->draft_logits, p.d_stride));
-    t.num_drafts = a->num_drafts;
-    t.temperature = a->temperature;
-    t.top_k = a->top_k;
-    t.seg_lists = reinterpret_cast<float2*>(scratch + TL.seg_lists);
-    t.seg_count = reinterpret_cast<int*>(scratch + TL.seg_count);
-    t.lists = reinterpret_cast<float2*>(scratch + TL.lists);
-    t.mz = reinterpret_cast<float2*>(scratch + TL.mz);
-    t.row_done = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + L.topk_done);
-    const int64_t items = static_cast<int64_t>(a->B) * (2 * a->K + 1) * TL.n_seg;
-    const int64_t ctas = std::min<int64_t>((items + kTkWarps - 1) / kTkWarps,
-                                             static_cast<int64_t>(kTkCtasPerSm) * dev.sms);
-    const sv_status ts = launch_topk(t, static_cast<int>(ctas), st);
+    const sv_status ts = run_topk_pass(a, workspace, L, TL, dev, st);
     if (ts != SV_OK) return ts;
   }
   // control CTAs (finalizes and draw finalizes, on SMs that stream nothing):
@@ -525,7 +578,8 @@ sv_status sv_row_stats(const sv_chain_args* a, float* alpha, float* expected, vo
                        size_t ws_bytes, sv_stream_t stream) {
   if (a == nullptr) return SV_EINVAL;
   if (a->B < 0 || a->B > SV_MAX_B || a->K < 0 || a->K > SV_MAX_K || a->V < 1 ||
-      a->V > SV_MAX_V || (a->dtype != SV_BF16 && a->dtype != SV_FP32))
+      a->V > SV_MAX_V || (a->dtype != SV_BF16 && a->dtype != SV_FP32) || a->max_top_k < 0 ||
+      a->max_top_k > SV_MAX_TOPK)
     return SV_EINVAL;
   if (a->B == 0) return SV_OK;
   if (a->target_logits == nullptr || a->target_row_stride < a->V || a->temperature == nullptr ||
@@ -533,18 +587,56 @@ sv_status sv_row_stats(const sv_chain_args* a, float* alpha, float* expected, vo
     return SV_EINVAL;
   if (a->K > 0 && (a->draft_logits == nullptr || a->draft_row_stride < a->V || alpha == nullptr))
     return SV_EINVAL;
-  const Layout L = layout_for(0, 0, 0);
+  const bool with_topk = a->top_k != nullptr && a->max_top_k > 0;
+  const Layout L0 = layout_for(0, 0, 0);
+  const size_t need =
+      with_topk ? sv_chain_workspace_bytes(a->B, a->K, a->V, a->dtype, a->max_top_k) : L0.jobs;
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0 ||
-      ws_bytes < L.jobs)
+      ws_bytes < need)
     return SV_EWORKSPACE;
   DeviceInfo dev;
   const sv_status ds = device_info(dev);
   if (ds != SV_OK) return ds;
   const int es = es_of(a->dtype);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (with_topk && a->K > 0) {
+    // filtered sampled requests: the top-k lists, then their statistics
+    const Layout L = chain_layout(a->B, a->K, a->V, a->dtype, a->max_top_k);
+    const TopkLayout TL = topk_layout(a->B, a->K, a->V, a->max_top_k);
+    const sv_status ts = run_topk_pass(a, workspace, L, TL, dev, s);
+    if (ts != SV_OK) return ts;
+    char* scratch = static_cast<char*>(workspace) + L.scratch;
+    StatsTopkProblem q;
+    q.B = a->B;
+    q.K = a->K;
+    q.V = a->V;
+    q.max_topk = a->max_top_k;
+    q.has_draft = true;
+    q.num_drafts = a->num_drafts;
+    q.temperature = a->temperature;
+    q.top_k = a->top_k;
+    q.lists = reinterpret_cast<float2*>(scratch + TL.lists);
+    q.mz = reinterpret_cast<float2*>(scratch + TL.mz);
+    q.alpha = alpha;
+    q.expected = expected;
+    q.hdr = static_cast<WsHeader*>(workspace);
+    // programmatic stream serialisation: the kernel waits for the top-k pass
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((a->B + kStTkWarps - 1) / kStTkWarps));
+    cfg.blockDim = dim3(kStTkWarps * 32);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, row_stats_topk_kernel, q) != cudaSuccess) return SV_ECUDA;
+  }
   StatsProblem p;
   p.B = a->B;
   p.K = a->K;
   p.V = a->V;
+  p.max_topk = with_topk ? a->max_top_k : 0;
   p.target = static_cast<const char*>(a->target_logits);
   p.t_stride = a->target_row_stride * es;
   p.draft = a->K > 0 ? static_cast<const char*>(a->draft_logits) : p.target;
@@ -557,10 +649,9 @@ sv_status sv_row_stats(const sv_chain_args* a, float* alpha, float* expected, vo
   p.alpha = alpha;
   p.expected = expected;
   p.hdr = static_cast<WsHeader*>(workspace);
-  p.tickets = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + L.tickets);
+  p.tickets = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + L0.tickets);
   const unsigned grid = static_cast<unsigned>(a->B) * static_cast<unsigned>(std::max(a->K, 1)) *
                         static_cast<unsigned>(kStCluster);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (es == 2) row_stats_kernel<2><<<grid, kStThreads, 0, s>>>(p);
   else row_stats_kernel<4><<<grid, kStThreads, 0, s>>>(p);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;

@@ -23,6 +23,13 @@
 //
 // The rank-0 CTA of the last pair of a request to finish (a counter per
 // request in the workspace, reset afterwards) adds up the expected tokens.
+//
+// Sampled requests with a top-k filter ("LLM speculative decoding study
+// notes 02", sec. 5.4: p and q each keep their own k most likely tokens)
+// take another route: the chain's top-k pass (sv_topk.cuh) reduces their
+// rows to (logit, id) lists and (m, Z), and row_stats_topk_kernel, one warp
+// per request, sums min(p, q) over the tokens both lists hold -- elsewhere
+// one of the two is zero.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -38,6 +45,7 @@ constexpr int kStSlots = 8;    // 16-byte vectors per row a thread keeps in regi
 
 struct StatsProblem {
   int B, K, V;
+  int max_topk;      // bound on top_k with top-k lists in the workspace (0: none)
   bool vec;          // 16-byte aligned rows, strides and row lengths
   const char* target;
   int64_t t_stride;  // bytes
@@ -100,7 +108,11 @@ __global__ void __cluster_dims__(kStCluster, 1, 1) __launch_bounds__(kStThreads)
   const int nd = a.num_drafts ? a.num_drafts[b] : a.K;
   const float t = a.temperature[b];
   const int tk = a.top_k ? a.top_k[b] : 0;
-  if (nd < 0 || nd > a.K || !(t >= 0.f) || tk < 0 || (tk > 0 && tk < a.V)) {
+  // a sampled request with a top-k filter takes its statistics from the
+  // top-k lists (row_stats_topk_kernel); without lists it is an error
+  const bool filtered = t > 0.f && tk > 0 && tk < a.V;
+  if (filtered && tk <= a.max_topk && nd >= 0 && nd <= a.K) return;
+  if (nd < 0 || nd > a.K || !(t >= 0.f) || tk < 0 || filtered) {
     if (i == 0 && rank == 0) {
       for (int j = tid; j < a.K; j += kStThreads) a.alpha[static_cast<size_t>(b) * a.K + j] = nanf;
       if (tid == 0) {
@@ -355,6 +367,109 @@ __global__ void __cluster_dims__(kStCluster, 1, 1) __launch_bounds__(kStThreads)
       a.tickets[b] = 0u;
     }
   }
+}
+
+// Statistics of top-k requests from the top-k lists: row (b, i) of the lists
+// is target row i for i <= nd and draft row i - nd - 1 after that, each its
+// k largest logits in token order with (m, Z) over them (sv_topk.cuh).  One
+// warp per request; p_i(x) = 2^((l - m) c) / Z on p_i's list and 0 off it,
+// likewise q_i, so alpha_i = sum over the ids on both lists of min(p_i, q_i),
+// in fp64.  Leaves the request's lists and (m, Z) zero, as the chain
+// finalize does.
+constexpr int kStTkWarps = 4;
+
+struct StatsTopkProblem {
+  int B, K, V, max_topk;
+  bool has_draft;
+  const int* num_drafts;
+  const float* temperature;
+  const int* top_k;
+  float2* lists;  // [B (2K+1)][max_topk]
+  float2* mz;     // [B (2K+1)]
+  float* alpha;
+  float* expected;
+  WsHeader* hdr;
+};
+
+__global__ void __launch_bounds__(kStTkWarps * 32) row_stats_topk_kernel(const StatsTopkProblem a) {
+  __shared__ int q_ids[kStTkWarps][SV_MAX_TOPK];
+  __shared__ float q_val[kStTkWarps][SV_MAX_TOPK];
+  grid_dependency_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = static_cast<int>(blockIdx.x) * kStTkWarps + warp;
+  if (b >= a.B) return;
+  const int nd = a.num_drafts ? a.num_drafts[b] : a.K;
+  const float t = a.temperature[b];
+  const int k = a.top_k ? a.top_k[b] : 0;
+  if (chain_kind(nd, t, k, a.K, a.V, a.max_topk, a.has_draft) != KIND_TOPK) return;
+  const int R = 2 * a.K + 1;
+  const size_t r0 = static_cast<size_t>(b) * R;
+  const int nrows = 2 * nd + 1;
+  const Scale2 c = scale_for(t);
+  const double cd = static_cast<double>(c.hi) + static_cast<double>(c.lo);
+  int err = 0;
+  for (int j = lane; j < nrows; j += 32) {
+    const float2 v = a.mz[r0 + j];
+    if (v.x != v.x) err |= SV_DERR_NONFINITE;
+    else if (v.x == kNegInf || !(v.y > 0.f)) err |= SV_DERR_MASS;
+  }
+  err = __reduce_or_sync(0xffffffffu, err);
+  double e = 1.0, reach = 1.0;
+  for (int i = 0; i < nd && !err; ++i) {
+    const float2* pl = a.lists + (r0 + i) * a.max_topk;
+    const float2* ql = a.lists + (r0 + nd + 1 + i) * a.max_topk;
+    const float2 mzp = a.mz[r0 + i], mzq = a.mz[r0 + nd + 1 + i];
+    for (int s = lane; s < k; s += 32) {
+      const float2 v = ql[s];
+      q_ids[warp][s] = __float_as_int(v.y);
+      q_val[warp][s] = v.x;
+    }
+    __syncwarp();
+    double acc = 0.0;
+    for (int s = lane; s < k; s += 32) {
+      const float2 v = pl[s];
+      const int id = __float_as_int(v.y);
+      // q's list is in token order: binary search for id
+      int lo = 0, hi = k - 1, at = -1;
+      while (lo <= hi && id >= 0) {
+        const int mid = (lo + hi) >> 1;
+        const int qm = q_ids[warp][mid];
+        if (qm == id) {
+          at = mid;
+          break;
+        }
+        if (qm < id) lo = mid + 1;
+        else hi = mid - 1;
+      }
+      if (at >= 0) {
+        const double pp = exp2_nonpos((static_cast<double>(v.x) - mzp.x) * cd) / mzp.y;
+        const double qq = exp2_nonpos((static_cast<double>(q_val[warp][at]) - mzq.x) * cd) / mzq.y;
+        acc += pp < qq ? pp : qq;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) a.alpha[static_cast<size_t>(b) * a.K + i] = static_cast<float>(acc);
+    reach *= acc;
+    e += reach;
+    __syncwarp();
+  }
+  if (lane == 0) {
+    if (err) {
+      for (int i = 0; i < a.K; ++i) a.alpha[static_cast<size_t>(b) * a.K + i] = __int_as_float(0x7fc00000);
+      a.expected[b] = __int_as_float(0x7fc00000);
+      record_error(&a.hdr->error, err);
+    } else {
+      for (int i = nd; i < a.K; ++i) a.alpha[static_cast<size_t>(b) * a.K + i] = __int_as_float(0x7fc00000);
+      a.expected[b] = static_cast<float>(e);
+    }
+  }
+  // leave the lists and (m, Z) of the request's rows zero
+  for (int j = 0; j < nrows; ++j) {
+    float2* l = a.lists + (r0 + j) * a.max_topk;
+    for (int s = lane; s < a.max_topk; s += 32) l[s] = make_float2(0.f, 0.f);
+  }
+  for (int j = lane; j < nrows; j += 32) a.mz[r0 + j] = make_float2(0.f, 0.f);
 }
 
 }  // namespace sv

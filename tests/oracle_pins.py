@@ -10,6 +10,9 @@ Which pin covers which oracle function:
                   check_greedy_* , the worked examples
   svo_residual    check_residual_lemma1, the worked examples
   svo_icdf        check_icdf_intervals, the worked examples, Monte Carlo
+  svo_icdf_window check_icdf_window_examples (dyadic weights, exact sums),
+                  check_icdf_window_bruteforce (the draws at a grid of
+                  uniforms), check_chain_draw_window
   svo_verify_chain  worked examples, check_grid_one_position (exact output
                   law = p), check_mc_chain (accept-length law, per-position
                   law, E[N]), check_greedy_spec_on_off, check_ragged
@@ -180,6 +183,69 @@ def check_icdf_intervals(lib):
     assert m < 1e-8  # near the boundary between ids 1 and 3
     tok, m = oracle.icdf(np.zeros(4), 0.5, lib=lib)
     assert tok == -1
+
+
+def check_icdf_window_examples(lib):
+    """svo_icdf_window on dyadic weights, where every sum is exact: the
+    tokens whose CDF step meets [u S - r S, u S + r S]."""
+    w = np.array([0.0, 2.0, 0.0, 1.0, 1.0])  # S = 4, steps at 2 (id 1), 3 (id 3), 4 (id 4)
+    cases = [
+        (0.5, 0.0, (3, 3, 1)),     # u S = 2 sits on the 1|3 step: the draw is 3
+        (0.5, 0.01, (1, 3, 2)),    # [1.96, 2.04] meets ids 1 and 3 (id 2 has no weight)
+        (0.5, 0.3, (1, 4, 3)),     # [0.8, 3.2] meets 1, 3 and 4
+        (0.999, 0.01, (4, 4, 1)),  # [3.956, 4.036]: the last step only
+        (0.0, 0.1, (1, 1, 1)),     # [-0.4, 0.4]: id 0 has no weight
+        (0.74, 0.02, (3, 4, 2)),   # [2.88, 3.04] meets 3 and 4
+    ]
+    for u, r, want in cases:
+        got = oracle.icdf_window(w, u, r, lib=lib)
+        assert got == want, (u, r, got, want)
+        if r == 0.0:
+            assert got[0] == oracle.icdf(w, u, lib=lib)[0]
+    assert oracle.icdf_window(np.zeros(3), 0.5, 0.1, lib=lib) == (-1, -1, -1)
+
+
+def check_icdf_window_bruteforce(lib):
+    """The window against the draws themselves: on random small weight
+    vectors (every positive weight at least 1e-3 of the total), the
+    inverse-CDF token at both ends of [u - r, u + r] and on a grid 1e-4
+    apart inside it hits every token whose step meets the window, and only
+    those."""
+    rng = np.random.default_rng(41)
+    for case in range(120):
+        V = int(rng.integers(2, 10))
+        w = rng.dirichlet(np.ones(V)) + 2e-2
+        w[rng.random(V) < 0.3] = 0.0
+        if not w.any():
+            w[rng.integers(V)] = 1.0
+        u = float(rng.random())
+        r = float(rng.choice([0.0, 1e-3, 0.02, 0.1]))
+        us = np.concatenate([[u - r, u + r], np.arange(u - r, u + r, 1e-4)])
+        hit = {oracle.icdf(w, float(x), lib=lib)[0] for x in us if 0.0 <= x < 1.0}
+        if u - r < 0.0:
+            hit.add(oracle.icdf(w, 0.0, lib=lib)[0])
+        if u + r >= 1.0:
+            hit.add(int(np.nonzero(w)[0][-1]))
+        lo, hi, n = oracle.icdf_window(w, u, r, lib=lib)
+        assert (lo, hi) == (min(hit), max(hit)), (case, w, u, r, lo, hi, sorted(hit))
+        assert n == int((w[lo:hi + 1] > 0).sum()) == len(hit), (case, n, sorted(hit))
+
+
+def check_chain_draw_window(lib):
+    """The chain reports the window of a near draw: [N02] sec. 9's round
+    (residual (0, .75, .25, 0, 0) after position 3 rejects).  A final
+    uniform 1e-8 below the 0.75 step is near and may give id 1 or 2; one at
+    0.5 is not near and gives id 1 alone."""
+    g = golden("n02_sec9_worked_round.json")
+    p, q, K = g["p"], g["q"], g["K"]
+    t, d = _chain_rows([p] * (K + 1), [q] * K)
+    r = list(g["accept_uniforms"])
+    r[1] = 0.999
+    near = oracle.verify_chain(t, d, [g["drafts"]], [1.0], [r + [0.75 - 1e-8]], lib=lib)
+    assert near["out_tokens"][0][2] == 1 and near["margin_draw"][0] < 1e-6
+    assert (near["draw_lo"][0], near["draw_hi"][0]) == (1, 2)
+    far = oracle.verify_chain(t, d, [g["drafts"]], [1.0], [r + [0.5]], lib=lib)
+    assert (far["draw_lo"][0], far["draw_hi"][0]) == (1, 1)
 
 
 def check_row_probs_softmax(lib):
@@ -901,6 +967,7 @@ def check_row_stats_tv(lib):
         assert abs(out["expected"][b] - e) < 1e-12
 
 
+ALL_FAST += [check_icdf_window_examples, check_icdf_window_bruteforce, check_chain_draw_window]
 ALL_FAST += [check_tree_noreplace_thresholds, check_tree_naive_examples,
              check_tree_modes_agree_when_greedy, check_tree_mask_slides,
              check_tree_mask_closure, check_row_stats_worked, check_row_stats_tv]

@@ -24,11 +24,12 @@ ATOL_ALPHA = 2e-5
 RTOL_EXPECTED = 1e-4
 
 
-def run_stats(inp, ws=None, target=None, draft=None):
+def run_stats(inp, ws=None, target=None, draft=None, max_top_k=None):
     out = sv.row_stats(target if target is not None else dev(inp["target"]),
                        draft if draft is not None else dev(inp["draft"]),
                        dev(inp["temperature"]), num_drafts=dev(inp["num_drafts"]),
-                       top_k=dev(inp["top_k"]) if inp["top_k"].any() else None, ws=ws)
+                       top_k=dev(inp["top_k"]) if inp["top_k"].any() else None, ws=ws,
+                       max_top_k=max_top_k)
     torch.cuda.synchronize()
     return {k: v.cpu().numpy() for k, v in out.items()}
 
@@ -83,14 +84,43 @@ def test_stats_no_drafts():
     assert np.all(got["expected"] == 1.0)
 
 
+def test_stats_topk_workload_shape():
+    """Workload 5's shape (K=8, V=152064 bf16, t=0.7, top-k 50 on p and
+    q): alpha_i is the sum of min(p_i, q_i) over the tokens both kept sets
+    hold, from the top-k pass's lists."""
+    inp = wl.make_chain(5, B=24)
+    got, ref = check_stats(inp)
+    assert 0.0 < ref["alpha"].mean() < 1.0
+
+
+def test_stats_topk_mixed_batch():
+    """Filtered and unfiltered, greedy and sampled requests in one call,
+    ragged drafts, ties at the k-th logit (rows of equal logits), and
+    k = 1 and k = 64."""
+    rng = np.random.default_rng(67)
+    B = 16
+    nd = rng.integers(0, 5, B).astype(np.int32)
+    inp = wl.make_chain(5, B=B, K=4, V=9000, num_drafts=nd, seed=68)
+    inp["top_k"] = rng.choice([0, 1, 7, 50, 64], B).astype(np.int32)
+    inp["temperature"] = rng.choice([0.0, 0.7, 1.1], B).astype(np.float32)
+    inp["target"][3, :, 100:200] = inp["target"][3, :, 150:151]   # a run of equal logits
+    inp["draft"][3, :, 100:200] = inp["draft"][3, :, 150:151]
+    check_stats(inp)
+    ws = sv.workspace(sv.sv_chain_workspace_bytes(B, 4, 9000, sv.SV_BF16, 64), "cuda", "stk")
+    for _ in range(2):  # the lists are left zero for the next call on the workspace
+        check_stats(inp, ws=ws)
+        from gpu_util import check_chain
+        check_chain(inp, ws=ws)
+
+
 def test_stats_data_errors():
     inp = wl.make_chain(2, B=6, V=2000, seed=64)
     inp["target"][1, 2, 77] = 0x7FC0      # NaN
     inp["draft"][2, 0, :] = 0xFF80        # a draft row with no mass
     inp["temperature"][3] = -1.0
-    inp["top_k"][4] = 20                  # top-k filtering: not supported here
+    inp["top_k"][4] = 20                  # top-k filtering without lists (max_top_k 0)
     ws = sv.workspace(sv.sv_chain_workspace_bytes(6, 4, 2000, sv.SV_BF16), "cuda", "stats_err")
-    got = run_stats(inp, ws=ws)
+    got = run_stats(inp, ws=ws, max_top_k=0)
     st, flags = sv.sv_get_error(ws)
     assert st == sv.SV_EDATA
     assert flags & sv.SV_DERR_NONFINITE and flags & sv.SV_DERR_MASS and flags & sv.SV_DERR_ARG

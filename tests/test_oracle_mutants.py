@@ -52,6 +52,10 @@ MUTANTS = {
                         "if (j != i) mrow[(size_t)i * W + j / 32] |= 1u << (j % 32);"),
     "mask_depth_off_by_one": ("      int d = -1;", "      int d = 0;"),
     "stats_sum_of_max": ("a += p[t] < q[t] ? p[t] : q[t];", "a += p[t] > q[t] ? p[t] : q[t];"),
+    "window_ignores_radius": ("const double a = (u - radius) * S, b = (u + radius) * S;",
+                              "const double a = u * S, b = u * S;"),
+    "window_keeps_zero_weights": ("    if (!(w[t] > 0.0)) continue;\n    if (c > a && c_prev <= b) {",
+                                  "    if (c > a && c_prev <= b) {"),
     "stats_expected_stops_early": ("for (int j = 0; j <= nd; ++j) {",
                                    "for (int j = 0; j < nd; ++j) {"),
 }

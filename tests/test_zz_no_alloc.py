@@ -1,18 +1,23 @@
 """The allocation-free chain entry point, sv_verify_chain_noalloc, against
-the workspace entry point sv_verify_chain on the same inputs.
+the fp64 oracle and against the workspace entry point sv_verify_chain on the
+same inputs.
 
 Its scratch is the library's per-device static array; the test checks that
-two calls in a row both give the workspace call's results (tokens and
-lengths bit for bit, probabilities within 1e-5 relative), and that a call
-too large for the scratch is refused before any device work.  This file is
-collected last so that it also runs after every other GPU test.
+two calls in a row both meet the oracle's parity bar (tests/gpu_util.py)
+and give the workspace call's results (tokens and lengths bit for bit,
+probabilities within 1e-5 relative), and that a call too large for the
+scratch is refused before any device work.  This file is collected last so
+that it also runs after every other GPU test.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import speculative_decoding_verification_63_gb300 as sv
 from speculative_decoding_verification_63_gb300 import workloads as wl
+
+from gpu_util import compare
 
 pytestmark = pytest.mark.gpu
 
@@ -43,6 +48,7 @@ def test_noalloc_matches_workspace_entry(cfg, B):
                           d["uniforms"], num_drafts=d["num_drafts"], with_probs=True)
     torch.cuda.synchronize()
     sv.check_device_errors(sv.workspace(1, "cuda", "chain"))
+    want = oracle.verify_chain_inputs(inp)
     for call in range(2):
         o = _outputs(B, K)
         sv.sv_verify_chain_noalloc(d["target"], d["draft"], d["tokens"], d["temperature"],
@@ -51,6 +57,9 @@ def test_noalloc_matches_workspace_entry(cfg, B):
                                    p_at_draft=o["p_at"], q_at_draft=o["q_at"])
         st, flags = sv.sv_noalloc_get_error()
         assert st == sv.SV_OK, (call, st, flags)
+        got = {k: v.cpu().numpy() for k, v in o.items()}
+        got["p_at_draft"], got["q_at_draft"] = got.pop("p_at"), got.pop("q_at")
+        compare(got, want, K + 1, prefix_tokens=inp["tokens"], V=inp["V"])
         for k in ("out_tokens", "out_len", "accept_len"):
             assert torch.equal(o[k], ref[k]), (call, k)
         for k, rk in (("p_at", "p_at_draft"), ("q_at", "q_at_draft")):
