@@ -167,6 +167,12 @@ typedef struct {
  *
  * Layout: target row c of request b at (b*N + c) * target_row_stride,
  * draft row m at (b*M + m) * draft_row_stride.
+ *
+ * Each request is walked by one thread-block cluster that reads only the
+ * rows on its path (the target rows of the nodes it stands on, the draft
+ * rows its children are tested against, and the next step's rows ahead of
+ * time); rows too long for the cluster's shared memory (bf16 V above about
+ * 160 K) take a slower engine that reduces every row first.
  */
 typedef struct {
   int32_t B, N, M, V, max_depth;

@@ -12,6 +12,7 @@
 #include "sv_topk.cuh"
 #include "sv_tree.cuh"
 #include "sv_treemask.cuh"
+#include "sv_treewalk.cuh"
 
 namespace {
 
@@ -194,6 +195,70 @@ sv_status launch_topk(const TopkPass& t, int grid, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, topk_kernel, t);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
+    return SV_EUNSUPPORTED;
+  return e == cudaSuccess ? SV_OK : SV_ECUDA;
+}
+
+// Geometry of a tree call on the cluster walk (sv_treewalk.cuh): the
+// smallest power-of-two cluster whose slices are at most 16 KB (more CTAs
+// per request would only add barriers), and the shared memory of the row
+// cache and the two residual slices; ok == false when that does not fit
+// (then the streaming engine takes the call).
+struct TreeWalkPlan {
+  bool ok = false;
+  int CL = 1, Ls = 0, slot_bytes = 0;
+  size_t smem = 0;
+};
+
+TreeWalkPlan tree_walk_plan(int64_t V, int es) {
+  TreeWalkPlan w;
+  const int64_t E = 16 / es;
+  int CL = 1;
+  while (CL < kTwMaxCl && ((V + CL - 1) / CL) * es > 16 * 1024) CL *= 2;
+  const int64_t Ls = ((V + CL - 1) / CL + E - 1) / E * E;
+  const int64_t slot = (Ls * es + 127) / 128 * 128;
+  const int64_t smem = kTwSlots * slot + 2 * ((Ls + 31) / 32 * 32) * 4;
+  if (smem > 200 * 1024) return w;
+  w.ok = true;
+  w.CL = CL;
+  w.Ls = static_cast<int>(Ls);
+  w.slot_bytes = static_cast<int>(slot);
+  w.smem = static_cast<size_t>(smem);
+  return w;
+}
+
+template <int ES>
+sv_status launch_tree_walk(const TreeWalkProblem& p, const TreeWalkPlan& wp, cudaStream_t stream) {
+  if (cudaFuncSetAttribute(tree_walk_kernel<ES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(wp.smem)) != cudaSuccess)
+    return SV_ECUDA;
+  if (wp.CL > 8 && cudaFuncSetAttribute(tree_walk_kernel<ES>,
+                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                       cudaSuccess)
+    return SV_ECUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(wp.CL));
+  cfg.blockDim = dim3(kTwThreads);
+  cfg.dynamicSmemBytes = wp.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(wp.CL);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int maxc = 0;
+  if (cudaOccupancyMaxActiveClusters(&maxc, tree_walk_kernel<ES>, &cfg) != cudaSuccess || maxc < 1)
+    return SV_ECUDA;
+  const int clusters = std::min(maxc, p.B);
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * wp.CL));
+  cfg.numAttrs = 2;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, tree_walk_kernel<ES>, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
     return SV_EUNSUPPORTED;
@@ -474,6 +539,43 @@ sv_status sv_verify_tree(const sv_tree_args* a, void* workspace, size_t ws_bytes
   if (ds != SV_OK) return ds;
 
   const int es = es_of(a->dtype);
+  const TreeWalkPlan wp = tree_walk_plan(a->V, es);
+  if (wp.ok) {
+    // the cluster walk: one cluster per request, reading only the rows on
+    // the path
+    TreeWalkProblem w;
+    w.B = a->B;
+    w.N = a->N;
+    w.M = a->M;
+    w.V = a->V;
+    w.max_depth = a->max_depth;
+    w.es = es;
+    w.mode = static_cast<int>(a->mode);
+    w.Ls = wp.Ls;
+    w.slot_bytes = wp.slot_bytes;
+    w.target = static_cast<const char*>(a->target_logits);
+    w.t_stride = a->target_row_stride * es;
+    w.draft = static_cast<const char*>(a->draft_logits);
+    w.d_stride = a->draft_logits ? a->draft_row_stride * es : 0;
+    w.bulk = bulk_ok(a->target_logits, w.t_stride, static_cast<int64_t>(a->V) * es) &&
+             (a->draft_logits == nullptr ||
+              bulk_ok(a->draft_logits, w.d_stride, static_cast<int64_t>(a->V) * es));
+    w.tokens = a->node_tokens;
+    w.parent = a->parent;
+    w.q_row = a->q_row;
+    w.num_nodes = a->num_nodes;
+    w.temperature = a->temperature;
+    w.top_k = a->top_k;
+    w.u_accept = a->u_accept;
+    w.u_sample = a->u_sample;
+    w.out_tokens = a->out_tokens;
+    w.out_len = a->out_len;
+    w.accept_len = a->accept_len;
+    w.accepted_nodes = a->accepted_nodes;
+    w.hdr = static_cast<WsHeader*>(workspace);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return es == 2 ? launch_tree_walk<2>(w, wp, st) : launch_tree_walk<4>(w, wp, st);
+  }
   const int chunk_el = chunk_el_of(a->dtype);
   const int ipr = (a->V + chunk_el - 1) / chunk_el;
   const Layout L = tree_layout(a->B, a->N, a->M, a->V, a->dtype);
