@@ -121,11 +121,13 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-# the sources each kernel is compiled from (the stored ncu figures are keyed
-# to them)
+# the sources each workload's dominant kernel is compiled from (the stored
+# ncu figures are keyed to them): the persistent chain kernel, the top-k
+# pass, the tree walk
 KERNEL_SOURCES = {
-    "chain": ("sv_device.cuh", "sv_rowpass.cuh", "sv_kernel.cuh", "sv_chain.cuh", "sv_topk.cuh"),
-    "tree": ("sv_device.cuh", "sv_rowpass.cuh", "sv_kernel.cuh", "sv_tree.cuh"),
+    "chain": ("sv_device.cuh", "sv_rowpass.cuh", "sv_kernel.cuh", "sv_chain.cuh"),
+    "topk": ("sv_device.cuh", "sv_rowpass.cuh", "sv_topk.cuh"),
+    "tree": ("sv_device.cuh", "sv_rowpass.cuh", "sv_cluster.cuh", "sv_treewalk.cuh"),
 }
 
 
@@ -277,6 +279,7 @@ class Workload:
         from speculative_decoding_verification_63_gb300 import workloads as wl
         self.key = key
         self.kind = "tree" if key == 4 else "chain"
+        self.kernel = {4: "tree", 5: "topk"}.get(key, "chain")  # the dominant kernel
         S = wl.SEED_BASE + key
         if key == 3:
             self.B = 64
@@ -794,7 +797,7 @@ def run_ours(args, dist):
     rounds_per_s = dist.world * wk.B * steps_per_s
     peak, peak_kind = hbm_peak()
     achieved = alg_mean / launch_s / 1e9
-    traffic = stored_traffic(wk.profile, wk.kind)
+    traffic = stored_traffic(wk.profile, wk.kernel)
 
     extra = {}
     if wk.key == 2 and dist.rank == 0:

@@ -21,6 +21,14 @@
  *   [DVP] "Speculative decoding: draft, verify and payoff", II.2 (the
  *         round, KV rollback to the rejected position).
  *
+ * Co-residency: the streaming engine's CTAs wait on one another's results
+ * (bounded waits), so it is launched cooperatively: every CTA of its grid
+ * (one per SM of the device) is resident at once, or the launch fails with
+ * SV_ECORESIDENT.  A caller that confines the library to part of the GPU
+ * (green contexts, MPS active-thread limits) gets that status rather than
+ * timeouts.  The cluster kernels (trees, top-k rows) wait only inside a
+ * cluster, which the hardware schedules as a unit.
+ *
  * Conventions for every entry point:
  *   - All array arguments are DEVICE pointers owned by the caller; the
  *     library allocates nothing and keeps no state between calls except what
@@ -57,7 +65,9 @@ typedef enum {
   SV_ETIMEOUT = 3,    /* a bounded device wait expired (see sv_get_error) */
   SV_EDATA = 4,       /* the data broke a precondition (see sv_get_error) */
   SV_EWORKSPACE = 5,  /* workspace null, too small or misaligned */
-  SV_EUNSUPPORTED = 6 /* no sm_103a device / kernel image for this device */
+  SV_EUNSUPPORTED = 6, /* no sm_103a device / kernel image for this device */
+  SV_ECORESIDENT = 7   /* the grid cannot be resident at once (fewer SMs free
+                          than the device has: a green context, MPS limits) */
 } sv_status;
 
 typedef enum { SV_BF16 = 0, SV_FP32 = 1 } sv_dtype;

@@ -14,7 +14,7 @@ import torch
 
 from ._build import LIBRARY
 
-SV_OK, SV_EINVAL, SV_ECUDA, SV_ETIMEOUT, SV_EDATA, SV_EWORKSPACE, SV_EUNSUPPORTED = range(7)
+SV_OK, SV_EINVAL, SV_ECUDA, SV_ETIMEOUT, SV_EDATA, SV_EWORKSPACE, SV_EUNSUPPORTED, SV_ECORESIDENT = range(8)
 SV_BF16, SV_FP32 = 0, 1
 SV_TREE_MSS, SV_TREE_MSS_NOREPLACE, SV_TREE_NAIVE = 0, 1, 2
 TREE_MODES = {"mss": SV_TREE_MSS, "noreplace": SV_TREE_MSS_NOREPLACE, "naive": SV_TREE_NAIVE}

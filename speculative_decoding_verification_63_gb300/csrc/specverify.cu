@@ -22,20 +22,19 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 struct Layout {
-  size_t tickets, jobs, topk_done, partials, segsums, scratch, total;
+  size_t tickets, jobs, partials, segsums, scratch, total;
 };
 
-// top-k pass: one counter per row (b, i) of a chain call
-constexpr size_t kTopkRows = static_cast<size_t>(SV_MAX_B) * (2 * SV_MAX_K + 1);
-
 static_assert(kDrawTicketBase == SV_MAX_B, "draw tickets follow the request tickets");
-static_assert(kTkMaxSegs * SV_MAX_TOPK <= kTkCap, "a row's segment lists fit one warp's buffer");
+static_assert(kTkCap >= kTkStep + SV_MAX_TOPK, "after an exact cut a whole step fits the buffer");
+static_assert(sizeof(TopkShared) * kTkCtasPerSm + 2048 <= 228 * 1024,
+              "the top-k pass keeps kTkCtasPerSm CTAs on an SM");
 static_assert(2 * SV_MAX_K + 1 <= 96, "top-k finalize: row statistics in three lanes' strides");
 static_assert(SV_MAX_V / kRSeg <= kMaxPages * kPageSeg && 2 * kMaxPages <= kMaxRowsPerReq,
               "draw finalize pages");
 
-// The header, the tickets (requests, then their draws), the draw records and
-// the top-k pass's row counters sit at fixed offsets with a fixed capacity
+// The header, the tickets (requests, then their draws) and the draw records
+// sit at fixed offsets with a fixed capacity
 // (SV_MAX_B requests), so the region that every call leaves zeroed is the
 // same for all problem sizes: one initialised workspace serves chain and
 // tree calls of any shape, one call at a time.
@@ -43,9 +42,8 @@ Layout layout_for(int64_t partial_slots, int64_t segsum_floats, int64_t scratch_
   Layout L;
   L.tickets = align_up(sizeof(WsHeader));
   L.jobs = align_up(L.tickets + sizeof(unsigned int) * 2 * static_cast<size_t>(SV_MAX_B));
-  L.topk_done = align_up(L.jobs + sizeof(unsigned long long) * kJobWords *
-                                      static_cast<size_t>(SV_MAX_B));
-  L.partials = align_up(L.topk_done + sizeof(unsigned int) * kTopkRows);
+  L.partials = align_up(L.jobs + sizeof(unsigned long long) * kJobWords *
+                                     static_cast<size_t>(SV_MAX_B));
   L.segsums = align_up(L.partials + sizeof(float2) * static_cast<size_t>(partial_slots));
   L.scratch = align_up(L.segsums + sizeof(float) * static_cast<size_t>(segsum_floats));
   L.total = align_up(L.scratch + sizeof(float) * static_cast<size_t>(scratch_floats));
@@ -68,26 +66,22 @@ int es_of(sv_dtype d) { return d == SV_BF16 ? 2 : 4; }
 int chunk_el_of(sv_dtype d) { return kChunkBytes / es_of(d); }
 int resid_chunk_el_of(sv_dtype d) { return kChunkBytes / 2 / es_of(d); }
 
-// Top-k pass: segments per row and their length, and the scratch it uses
-// (byte offsets within the scratch region): per row its list and (m, Z),
-// per segment its list and count.
+// Top-k pass: the length of a row's eight segments, and the scratch it
+// writes (byte offsets within the scratch region): per row its list and
+// (m, Z).
 struct TopkLayout {
-  int n_seg = 0, seg_len = 0;
-  size_t lists = 0, mz = 0, seg_lists = 0, seg_count = 0, bytes = 0;
+  int seg_len = 0;
+  size_t lists = 0, mz = 0, bytes = 0;
 };
 TopkLayout topk_layout(int64_t B, int64_t K, int64_t V, int64_t max_top_k) {
   TopkLayout T;
   if (max_top_k <= 0) return T;
-  const int64_t s0 = std::min<int64_t>(kTkMaxSegs, std::max<int64_t>(1, (V + kTkMinSeg - 1) / kTkMinSeg));
-  const int64_t per = (V + s0 - 1) / s0;
-  T.seg_len = static_cast<int>((per + kTkStep - 1) / kTkStep * kTkStep);
-  T.n_seg = static_cast<int>((V + T.seg_len - 1) / T.seg_len);  // every segment non-empty
+  const int64_t per = (V + kTkWarps - 1) / kTkWarps;
+  T.seg_len = static_cast<int>((per + kTkSegAlign - 1) / kTkSegAlign * kTkSegAlign);
   const size_t rows = static_cast<size_t>(B) * (2 * K + 1);
   T.lists = 0;
   T.mz = align_up(T.lists + sizeof(float2) * rows * max_top_k);
-  T.seg_lists = align_up(T.mz + sizeof(float2) * rows);
-  T.seg_count = align_up(T.seg_lists + sizeof(float2) * rows * T.n_seg * max_top_k);
-  T.bytes = align_up(T.seg_count + sizeof(int) * rows * T.n_seg);
+  T.bytes = align_up(T.mz + sizeof(float2) * rows);
   return T;
 }
 
@@ -149,23 +143,31 @@ sv_status launch(const P& prob, int grid, cudaStream_t stream) {
   if (cudaFuncSetAttribute(verify_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return SV_ECUDA;
-  // programmatic stream serialisation: the kernel waits for the preceding
+  // Programmatic stream serialisation: the kernel waits for the preceding
   // work itself (griddepcontrol.wait), so its launch may overlap that work's
-  // tail
+  // tail.  Cooperative: CTAs of this kernel wait on results other CTAs
+  // publish (control CTAs on chunk partials, draw scouts on draw records),
+  // so every CTA of the grid must be resident at once; a cooperative launch
+  // guarantees that, or fails up front (SV_ECORESIDENT) when the grid
+  // cannot fit -- e.g. when a green context or MPS leaves the call fewer SMs
+  // than the device reports -- instead of waiting out the bounded waits.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, verify_kernel<P>, prob);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
     return SV_EUNSUPPORTED;
+  if (e == cudaErrorCooperativeLaunchTooLarge) return SV_ECORESIDENT;
   return e == cudaSuccess ? SV_OK : SV_ECUDA;
 }
 
@@ -174,20 +176,16 @@ bool bulk_ok(const void* base, int64_t stride_bytes, int64_t row_bytes) {
          (stride_bytes & 15) == 0 && (row_bytes & 15) == 0;
 }
 
-// rows start on 16-byte boundaries (16-byte loads; a row's ragged end is
-// read element by element)
-bool aligned16(const void* base, int64_t stride_bytes) {
-  return base != nullptr && (reinterpret_cast<uintptr_t>(base) & 15) == 0 &&
-         (stride_bytes & 15) == 0;
-}
-
 sv_status launch_topk(const TopkPass& t, int grid, cudaStream_t stream) {
+  if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(sizeof(TopkShared))) != cudaSuccess)
+    return SV_ECUDA;
   // programmatic stream serialisation, as for the persistent kernel: the
   // pass waits for the preceding work itself
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(std::max(grid, 1)));
   cfg.blockDim = dim3(kTkThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = sizeof(TopkShared);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -278,26 +276,24 @@ sv_status run_topk_pass(const sv_chain_args* a, void* workspace, const Layout& L
   t.V = a->V;
   t.es = es;
   t.max_topk = a->max_top_k;
-  t.n_seg = TL.n_seg;
   t.seg_len = TL.seg_len;
   t.has_draft = a->draft_logits != nullptr;
   t.target = static_cast<const char*>(a->target_logits);
   t.t_stride = a->target_row_stride * es;
   t.draft = static_cast<const char*>(a->draft_logits);
   t.d_stride = a->draft_logits ? a->draft_row_stride * es : 0;
-  t.vec = aligned16(a->target_logits, t.t_stride) &&
-          (a->draft_logits == nullptr || aligned16(a->draft_logits, t.d_stride));
+  t.bulk = bulk_ok(a->target_logits, t.t_stride, static_cast<int64_t>(a->V) * es) &&
+           (a->draft_logits == nullptr ||
+            bulk_ok(a->draft_logits, t.d_stride, static_cast<int64_t>(a->V) * es));
   t.num_drafts = a->num_drafts;
   t.temperature = a->temperature;
   t.top_k = a->top_k;
-  t.seg_lists = reinterpret_cast<float2*>(scratch + TL.seg_lists);
-  t.seg_count = reinterpret_cast<int*>(scratch + TL.seg_count);
   t.lists = reinterpret_cast<float2*>(scratch + TL.lists);
   t.mz = reinterpret_cast<float2*>(scratch + TL.mz);
-  t.row_done = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + L.topk_done);
-  const int64_t items = static_cast<int64_t>(a->B) * (2 * a->K + 1) * TL.n_seg;
-  const int64_t ctas = std::min<int64_t>((items + kTkWarps - 1) / kTkWarps,
-                                         static_cast<int64_t>(kTkCtasPerSm) * dev.sms);
+  t.err = &ws_view(workspace, L).hdr->error;
+  // one CTA per row at a time, every CTA resident
+  const int64_t rows = static_cast<int64_t>(a->B) * (2 * a->K + 1);
+  const int64_t ctas = std::min<int64_t>(rows, static_cast<int64_t>(kTkCtasPerSm) * dev.sms);
   return launch_topk(t, static_cast<int>(ctas), st);
 }
 
@@ -407,6 +403,8 @@ const char* sv_status_string(sv_status s) {
     case SV_EDATA: return "SV_EDATA: input data broke a precondition";
     case SV_EWORKSPACE: return "SV_EWORKSPACE: workspace missing, too small or misaligned";
     case SV_EUNSUPPORTED: return "SV_EUNSUPPORTED: needs an sm_103 (GB300) device";
+    case SV_ECORESIDENT:
+      return "SV_ECORESIDENT: the kernel's CTAs cannot all be resident at once on this device";
   }
   return "unknown sv_status";
 }

@@ -98,6 +98,12 @@ __device__ __forceinline__ void bulk_copy_g2s(void* smem_dst, const void* gmem_s
       : "memory");
 }
 
+// Order this thread's earlier generic-proxy accesses to shared memory
+// before later async-proxy ones (a bulk copy into a buffer just read).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -126,9 +132,19 @@ __device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Named barrier over the first `count` threads of the block.
+// Named barrier over the first `count` threads of the block (whole,
+// converged warps: the caller reconverges after divergent code).
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// Arrive on a named barrier without waiting (the producer side of a
+// hand-over: this warp's earlier writes are visible to the threads that
+// wait on the barrier with named_sync).  The barrier counts whole warps,
+// so the warp is reconverged first: a lane still inside a branch would
+// otherwise be counted as arrived before its writes.
+__device__ __forceinline__ void named_arrive(uint32_t id, uint32_t count) {
+  __syncwarp();
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ------------------------------------------------------------------ values

@@ -157,10 +157,24 @@ def test_host_side_checks(svlib):
 
 def test_status_strings(svlib):
     from speculative_decoding_verification_63_gb300 import _binding as b
-    names = [b.sv_status_string(s) for s in range(7)]
+    names = [b.sv_status_string(s) for s in range(8)]
     assert names[0] == "SV_OK" and all(n.startswith("SV_E") for n in names[1:])
-    assert len(set(names)) == 7
+    assert len(set(names)) == 8
+    assert names[b.SV_ECORESIDENT].startswith("SV_ECORESIDENT")
     assert b.sv_version() >= 100
+
+
+def test_status_codes_match_the_header():
+    """Every status the header defines (among them SV_ECORESIDENT, the
+    answer to a grid that cannot be resident at once) has the same value in
+    the binding."""
+    import re
+    from speculative_decoding_verification_63_gb300 import _binding as b
+    text = open(os.path.join(ROOT, "include", "specverify.h")).read()
+    enum = dict(re.findall(r"\b(SV_OK|SV_E[A-Z]+)\s*=\s*(\d+)", text))
+    assert "SV_ECORESIDENT" in enum and len(enum) == 8
+    for name, value in enum.items():
+        assert getattr(b, name) == int(value), name
 
 
 def test_product_has_no_cpu_fallback():
