@@ -25,19 +25,36 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA 13 toolkit is required to build libspecverify")
 
 
-def build_library(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+def compile_flags(nvtx: bool = False, extra_flags=()) -> list[str]:
+    """nvcc flags of the library build; nvtx adds the NVTX ranges around the
+    entry points (-DSV_NVTX)."""
+    return [*ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
+            "-cudart", "shared", "-Xlinker", "-rpath,/usr/local/cuda/lib64", f"-I{INCLUDE}",
+            *(["-DSV_NVTX"] if nvtx else []), *extra_flags]
+
+
+def build_library(force: bool = False, verbose: bool = False, extra_flags=(),
+                  nvtx: bool | None = None) -> str:
     """Compile csrc/specverify.cu into libspecverify.so (one translation
-    unit, -O3, IEEE division and sqrt, no fast-math)."""
+    unit, -O3, IEEE division and sqrt, no fast-math).  nvtx (default: the
+    environment variable SV_NVTX=1) builds the traced variant; a change of
+    flags forces a rebuild."""
+    if nvtx is None:
+        nvtx = os.environ.get("SV_NVTX", "") == "1"
+    flags = compile_flags(nvtx, extra_flags)
+    stamp = LIBRARY + ".flags"
     newest = max(os.path.getmtime(p) for p in sources() + [os.path.join(INCLUDE, "specverify.h")])
-    if not force and os.path.exists(LIBRARY) and os.path.getmtime(LIBRARY) >= newest:
+    same_flags = os.path.exists(stamp) and open(stamp).read() == " ".join(flags)
+    if (not force and same_flags and os.path.exists(LIBRARY)
+            and os.path.getmtime(LIBRARY) >= newest):
         return LIBRARY
     tmp = LIBRARY + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
-           "-cudart", "shared", "-Xlinker", "-rpath,/usr/local/cuda/lib64",
-           f"-I{INCLUDE}", "-o", tmp, os.path.join(CSRC, "specverify.cu"), *extra_flags]
+    cmd = [nvcc(), *flags, "-o", tmp, os.path.join(CSRC, "specverify.cu")]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
         print(" ".join(cmd))
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIBRARY)
+    with open(stamp, "w") as f:
+        f.write(" ".join(flags))
     return LIBRARY

@@ -7,6 +7,9 @@
 #include <mutex>
 
 #include "specverify.h"
+#ifdef SV_NVTX
+#include <nvtx3/nvToolsExt.h>
+#endif
 #include "sv_chain.cuh"
 #include "sv_stats.cuh"
 #include "sv_topk.cuh"
@@ -390,6 +393,20 @@ sv_status noalloc_scratch(cudaStream_t stream, void** out) {
 
 }  // namespace
 
+// Tracing (a build with -DSV_NVTX): every entry point that enqueues device
+// work opens an NVTX range named after it on the calling host thread, so a
+// timeline profiler shows where each call's launches were enqueued.  The
+// header-only NVTX library stays inert unless a profiler attaches.
+#ifdef SV_NVTX
+struct SvRange {
+  explicit SvRange(const char* name) { nvtxRangePushA(name); }
+  ~SvRange() { nvtxRangePop(); }
+};
+#define SV_RANGE(name) const SvRange sv_range_(name)
+#else
+#define SV_RANGE(name) static_cast<void>(0)
+#endif
+
 extern "C" {
 
 int32_t sv_version(void) { return 100; }
@@ -427,6 +444,7 @@ size_t sv_tree_workspace_bytes(int32_t B, int32_t N, int32_t M, int32_t V, sv_dt
 }
 
 sv_status sv_workspace_init(void* workspace, size_t ws_bytes, sv_stream_t stream) {
+  SV_RANGE("sv_workspace_init");
   if (workspace == nullptr || ws_bytes < sizeof(WsHeader)) return SV_EWORKSPACE;
   return cudaMemsetAsync(workspace, 0, ws_bytes, reinterpret_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
@@ -436,6 +454,7 @@ sv_status sv_workspace_init(void* workspace, size_t ws_bytes, sv_stream_t stream
 
 sv_status sv_verify_chain(const sv_chain_args* a, void* workspace, size_t ws_bytes,
                           sv_stream_t stream) {
+  SV_RANGE("sv_verify_chain");
   if (a == nullptr) return SV_EINVAL;
   if (a->B < 0 || a->B > SV_MAX_B || a->K < 0 || a->K > SV_MAX_K || a->V < 1 ||
       a->V > SV_MAX_V || (a->dtype != SV_BF16 && a->dtype != SV_FP32) || a->max_top_k < 0 ||
@@ -514,6 +533,7 @@ sv_status sv_verify_chain(const sv_chain_args* a, void* workspace, size_t ws_byt
 
 sv_status sv_verify_tree(const sv_tree_args* a, void* workspace, size_t ws_bytes,
                          sv_stream_t stream) {
+  SV_RANGE("sv_verify_tree");
   if (a == nullptr) return SV_EINVAL;
   if (a->B < 0 || a->B > SV_MAX_TREE_B || a->N < 1 || a->N > SV_MAX_TREE_NODES || a->M < 1 ||
       a->M > SV_MAX_TREE_NODES || a->V < 1 || a->V > SV_MAX_V || a->max_depth < 0 ||
@@ -615,6 +635,7 @@ sv_status sv_verify_tree(const sv_tree_args* a, void* workspace, size_t ws_bytes
 }
 
 sv_status sv_get_error(void* workspace, sv_stream_t stream, int32_t* device_flags) {
+  SV_RANGE("sv_get_error");
   if (workspace == nullptr) return SV_EWORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return SV_ECUDA;
@@ -648,6 +669,7 @@ sv_status sv_selftest_wait_timeout(void* workspace, size_t ws_bytes, int64_t lim
 
 sv_status sv_tree_mask(const sv_tree_mask_args* a, void* workspace, size_t ws_bytes,
                        sv_stream_t stream) {
+  SV_RANGE("sv_tree_mask");
   if (a == nullptr) return SV_EINVAL;
   if (a->B < 0 || a->B > SV_MAX_TREE_B || a->N < 1 || a->N > SV_MAX_TREE_NODES ||
       a->words < (a->N + 31) / 32 || a->words > 1 << 20)
@@ -676,6 +698,7 @@ sv_status sv_tree_mask(const sv_tree_mask_args* a, void* workspace, size_t ws_by
 
 sv_status sv_row_stats(const sv_chain_args* a, float* alpha, float* expected, void* workspace,
                        size_t ws_bytes, sv_stream_t stream) {
+  SV_RANGE("sv_row_stats");
   if (a == nullptr) return SV_EINVAL;
   if (a->B < 0 || a->B > SV_MAX_B || a->K < 0 || a->K > SV_MAX_K || a->V < 1 ||
       a->V > SV_MAX_V || (a->dtype != SV_BF16 && a->dtype != SV_FP32) || a->max_top_k < 0 ||
@@ -758,6 +781,7 @@ sv_status sv_row_stats(const sv_chain_args* a, float* alpha, float* expected, vo
 }
 
 sv_status sv_verify_chain_noalloc(const sv_chain_args* a, sv_stream_t stream) {
+  SV_RANGE("sv_verify_chain_noalloc");
   if (a == nullptr) return SV_EINVAL;
   if (a->B == 0) return sv_verify_chain(a, nullptr, 0, stream);
   const size_t need = sv_chain_workspace_bytes(a->B, a->K, a->V, a->dtype, a->max_top_k);
@@ -773,6 +797,7 @@ sv_status sv_verify_chain_noalloc(const sv_chain_args* a, sv_stream_t stream) {
 }
 
 sv_status sv_noalloc_get_error(sv_stream_t stream, int32_t* device_flags) {
+  SV_RANGE("sv_noalloc_get_error");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   void* ws = nullptr;
   const sv_status st = noalloc_scratch(s, &ws);

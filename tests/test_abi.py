@@ -190,3 +190,26 @@ def test_product_has_no_cpu_fallback():
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", txt, re.M), f
     with pytest.raises(RuntimeError):
         _binding.lib(os.path.join(pkg_dir, "does_not_exist.so"))
+
+
+def test_nvtx_build_opens_a_range_per_entry_point():
+    """The traced build (-DSV_NVTX) wraps every entry point that enqueues
+    device work in an NVTX range named after it (preprocessed only: the
+    ranges need no GPU)."""
+    import re
+    import subprocess
+    from speculative_decoding_verification_63_gb300 import _build
+    src = os.path.join(_build.CSRC, "specverify.cu")
+    flags = [f for f in _build.compile_flags(nvtx=True) if f.startswith(("-I", "-D", "-std"))]
+    out = subprocess.run([_build.nvcc(), "-E", "-x", "cu", *flags, src], capture_output=True,
+                         text=True, check=True).stdout
+    for name in ("sv_verify_chain", "sv_verify_tree", "sv_row_stats", "sv_tree_mask",
+                 "sv_verify_chain_noalloc", "sv_workspace_init"):
+        body = re.search(r"sv_status\s+" + name + r"\s*\([^{]*\{\s*const\s+SvRange\s+sv_range_\s*\(\s*\"" +
+                         name + r"\"\s*\)", out)
+        assert body, name
+    assert "nvtxRangePushA" in out
+    plain = subprocess.run([_build.nvcc(), "-E", "-x", "cu",
+                            *[f for f in _build.compile_flags() if f.startswith(("-I", "-D", "-std"))],
+                            src], capture_output=True, text=True, check=True).stdout
+    assert "SvRange" not in plain
