@@ -24,8 +24,8 @@
 //           L: a value that at least k logits of the row reach, so that
 //           nothing below it can be in the top-k.  The eight warps raise L
 //           together.  Every kept logit is counted in a histogram of the
-//           row that the CTA shares (2048 bins: sign, exponent and the top
-//           two mantissa bits of the logit), and L is the lower edge of
+//           row that the CTA shares (1/8-binade bins for positive logits,
+//           32 coarse bins below zero), and L is the lower edge of
 //           the highest bin at and above which k logits have been counted;
 //           a warp that finds a better L publishes it for the others.
 //           After the first few thousand tokens L sits just below the
@@ -68,7 +68,8 @@ constexpr int kTkCap = 32 * kTkCapLane;           // candidates a streaming warp
 constexpr int kTkStageBytes = 2048;               // one bulk copy
 constexpr int kTkStages = 3;                      // bulk copies in flight per streaming warp
 constexpr int kTkSegAlign = 64;                   // segment starts: multiples of 64 tokens
-constexpr int kTkBins = 2048;                     // the row histogram
+constexpr int kTkNegBins = 32;                    // row histogram: negative logits, coarse
+constexpr int kTkBins = kTkNegBins + 2048;        // and the rest in 1/8-binade bins
 // named barriers: + the set's parity, lists ready for the merge / set free
 // again; and the streaming warps among themselves
 constexpr uint32_t kTkBarFull = 1, kTkBarFree = 3, kTkBarStream = 5;
@@ -133,8 +134,19 @@ __device__ __forceinline__ float tk_value(unsigned key, int es) {
 __device__ __forceinline__ unsigned tk_key_of(float v, int es) {
   return es == 2 ? tk_key16(__float_as_uint(v) >> 16) : tk_key32(__float_as_uint(v));
 }
-// histogram bin of a key: sign, exponent and two mantissa bits
-__device__ __forceinline__ int tk_bin_shift(int es) { return es == 2 ? 5 : 21; }
+// Histogram bin of a key.  The bins that set L are those of the row's top
+// logits, which are positive in practice: a positive logit (or zero) gets
+// one of 2048 bins of 1/8 binade (its exponent and top three mantissa
+// bits); the negative logits share 32 coarse bins.  Monotone in the key.
+__device__ __forceinline__ unsigned tk_bin(unsigned key, int es) {
+  if (es == 2) return key < 0x8000u ? key >> 10 : kTkNegBins + ((key - 0x8000u) >> 4);
+  return key < 0x80000000u ? key >> 26 : kTkNegBins + ((key - 0x80000000u) >> 20);
+}
+// the lowest key of bin b
+__device__ __forceinline__ unsigned tk_bin_edge(unsigned b, int es) {
+  if (es == 2) return b < kTkNegBins ? b << 10 : 0x8000u + ((b - kTkNegBins) << 4);
+  return b < kTkNegBins ? b << 26 : 0x80000000u + ((b - kTkNegBins) << 20);
+}
 // the largest float below v (v > -inf, not NaN)
 __device__ __forceinline__ float tk_below(float v) {
   const unsigned u = __float_as_uint(v);
@@ -390,8 +402,7 @@ __device__ __forceinline__ void tk_refresh(TkWarp& w, const TkRowState& rs, bool
     n_seen = __shfl_sync(0xffffffffu, n_seen, 0);
     top_b = __shfl_sync(0xffffffffu, top_b, 0);
     if (n_seen >= static_cast<unsigned>(k)) {
-      const int shift = tk_bin_shift(es);
-      const int floor_b = static_cast<int>(lk >> shift);  // no gain at or below the bound's bin
+      const int floor_b = static_cast<int>(tk_bin(lk, es));  // no gain at or below the bound's bin
       const volatile unsigned* hist = rs.hist;
       int hi = static_cast<int>(top_b);
       unsigned carry = 0;
@@ -402,7 +413,7 @@ __device__ __forceinline__ void tk_refresh(TkWarp& w, const TkRowState& rs, bool
         const unsigned hit =
             __ballot_sync(0xffffffffu, b > floor_b && incl >= static_cast<unsigned>(k));
         if (hit) {
-          lk = static_cast<unsigned>(hi - (__ffs(hit) - 1)) << shift;
+          lk = tk_bin_edge(static_cast<unsigned>(hi - (__ffs(hit) - 1)), es);
           if (lane == 0) atomicMax(rs.lk, lk);
           break;
         }
@@ -521,7 +532,6 @@ __device__ __forceinline__ void tk_take(TkWarp& w, const uint4 (&raw)[ES], unsig
     }
   }
   if (cl) {
-    constexpr int shift = ES == 2 ? 5 : 21;
     unsigned mb = 0u;
     while (pass) {
       const int i = __ffs(pass) - 1;
@@ -535,7 +545,7 @@ __device__ __forceinline__ void tk_take(TkWarp& w, const uint4 (&raw)[ES], unsig
       w.key[lane + 32 * w.c] = kk;
       w.id[lane + 32 * w.c] = id0 + g * S::kSpan + lane * S::kEpg + j;
       ++w.c;
-      const unsigned b = kk >> shift;
+      const unsigned b = tk_bin(kk, ES);
       atomicAdd(rs.hist + b, 1u);
       mb = max(mb, b);
     }
