@@ -84,6 +84,9 @@ struct TwShared {
   uint4 xr[2][2];             // this CTA's exchange record (double-buffered)
   uint4 xall[kTwMaxCl][2];    // the cluster's records of the last exchange
   float red[4][kTwWarps];     // block-reduction scratch
+  int redf[kTwWarps];
+  float ua[kTwMaxNodes];      // the request's accept uniforms, and its sample uniform
+  float us;
   DF dscan[kTwWarps];
   int ibuf[4];
   int err;
@@ -113,6 +116,28 @@ __device__ __forceinline__ MS tw_block_ms(MS v, Scale2 c, TwShared& sh) {
   MS w = lane < kTwWarps ? MS{sh.red[0][lane], sh.red[1][lane]} : MS{kNegInf, 0.f};
   w = warp_reduce_ms(w, c);
   return w;
+}
+
+// Two block (max, sum) reductions and an OR of flags with one exchange
+// through shared memory; each pair combines exactly as tw_block_ms would.
+__device__ __forceinline__ int tw_block_ms2(MS& a, MS& b, int flag, Scale2 c, TwShared& sh) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  a = warp_reduce_ms(a, c);
+  b = warp_reduce_ms(b, c);
+  flag = __reduce_or_sync(0xffffffffu, flag);
+  __syncthreads();
+  if (lane == 0) {
+    sh.red[0][warp] = a.m;
+    sh.red[1][warp] = a.s;
+    sh.red[2][warp] = b.m;
+    sh.red[3][warp] = b.s;
+    sh.redf[warp] = flag;
+  }
+  __syncthreads();
+  const bool in = lane < kTwWarps;
+  a = warp_reduce_ms(in ? MS{sh.red[0][lane], sh.red[1][lane]} : MS{kNegInf, 0.f}, c);
+  b = warp_reduce_ms(in ? MS{sh.red[2][lane], sh.red[3][lane]} : MS{kNegInf, 0.f}, c);
+  return __reduce_or_sync(0xffffffffu, in ? sh.redf[lane] : 0);
 }
 
 __device__ __forceinline__ VI tw_block_vi(VI v, TwShared& sh) {
@@ -282,21 +307,97 @@ __global__ void __launch_bounds__(kTwThreads, 1) tree_walk_kernel(const TreeWalk
     }
     __syncwarp();
   };
-  // all threads: the slot of a row, once loaded (asked for now if no slot
-  // was free when it was prefetched: anything but the rows of the current
-  // step, ibuf[0..1], may make room)
+  // all threads: the slot of a row, once loaded.  The caller has passed a
+  // barrier since the cache table last changed, so every thread finds the
+  // same slot; a row that found no slot when it was prefetched is asked for
+  // now (anything but the rows of the current step, ibuf[0..1], may make
+  // room), between two barriers.
   auto acquire = [&](int b, int kind, int row) -> const unsigned char* {
-    __syncthreads();
-    if (warp == 0) {
-      const int keep[2] = {sh.ibuf[0], sh.ibuf[1]};
-      ensure(b, kind, row, keep, 2);
+    int s = find_slot(key_of(kind, row));
+    if (s < 0) {
+      __syncthreads();  // every thread has read the table
+      if (warp == 0) {
+        const int keep[2] = {sh.ibuf[0], sh.ibuf[1]};
+        ensure(b, kind, row, keep, 2);
+      }
+      __syncthreads();
+      s = find_slot(key_of(kind, row));
+      if (s < 0) return nullptr;
     }
-    __syncthreads();
-    const int s = find_slot(key_of(kind, row));
-    if (s < 0) return nullptr;
     if (!mbar_wait_bounded(&sh.bar[s], (sh.issued[s] - 1u) & 1u, tw_limit(sh)) && tid == 0)
       flag_timeout();
     return slots + static_cast<size_t>(s) * P.slot_bytes;
+  };
+
+  // warp 0: the rows wanted next (lane i < nw holds the i-th by priority:
+  // kind, row) put on their way into the cache, all at once, one lane per
+  // row.  A slot is reused only when its key is not wanted and its last load
+  // has landed, so nothing here waits; a wanted row left without a slot is
+  // loaded by acquire when it is needed.
+  auto prefetch = [&](int b, int nw, int wkind, int wrow) {
+    const int wkey = lane < nw ? key_of(wkind, wrow) : -2;
+    const int tg = lane < kTwSlots ? sh.tag[lane] : -3;
+    const bool idle = lane < kTwSlots &&
+                      (sh.issued[lane] == 0u ||
+                       mbar_test_wait(&sh.bar[lane], (sh.issued[lane] - 1u) & 1u));
+    bool present = false, wanted = false;
+#pragma unroll
+    for (int q = 0; q < kTwSlots; ++q) {
+      // both shuffles run in every lane (never inside a short-circuit)
+      const int tq = __shfl_sync(0xffffffffu, tg, q);
+      const int wq = __shfl_sync(0xffffffffu, wkey, q);
+      present |= lane < nw && tq == wkey;              // in a slot already
+      present |= lane < nw && q < lane && wq == wkey;  // an earlier lane asks for it
+      wanted |= q < nw && tg == wq;                    // slot `lane` holds a wanted row
+    }
+    const unsigned free_m = __ballot_sync(0xffffffffu, lane < kTwSlots && !wanted && idle);
+    const unsigned miss_m = __ballot_sync(0xffffffffu, lane < nw && !present);
+    int slot = -1;
+    if ((miss_m >> lane) & 1u) {
+      unsigned f = free_m;
+      for (int q = __popc(miss_m & ((1u << lane) - 1u)); q > 0 && f; --q) f &= f - 1u;
+      if (f) slot = __ffs(f) - 1;
+    }
+    const char* src = nullptr;
+    if (slot >= 0)
+      src = wkind == 0 ? P.target + (static_cast<int64_t>(b) * N + wrow) * P.t_stride +
+                             static_cast<int64_t>(lo) * ES
+                       : P.draft + (static_cast<int64_t>(b) * P.M + wrow) * P.d_stride +
+                             static_cast<int64_t>(lo) * ES;
+    if (slot >= 0) {
+      sh.tag[slot] = wkey;
+      sh.issued[slot] += 1u;
+      if (P.bulk) {
+        const uint32_t bytes = static_cast<uint32_t>(n_sl * ES);
+        mbar_arrive_expect_tx(&sh.bar[slot], bytes);
+        if (bytes > 0)
+          bulk_copy_g2s_hint(slots + static_cast<size_t>(slot) * P.slot_bytes, src, bytes,
+                             &sh.bar[slot], pol);
+      }
+    }
+    __syncwarp();
+    if (!P.bulk) {
+      // rows unfit for bulk copies: the warp copies the slices in turn
+      unsigned m = __ballot_sync(0xffffffffu, slot >= 0);
+      while (m) {
+        const int i = __ffs(m) - 1;
+        m &= m - 1u;
+        const int si = __shfl_sync(0xffffffffu, slot, i);
+        const char* sp = reinterpret_cast<const char*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(src), i));
+        unsigned char* dst = slots + static_cast<size_t>(si) * P.slot_bytes;
+        for (int e = lane; e < n_sl; e += 32) {
+          if constexpr (ES == 2)
+            reinterpret_cast<uint16_t*>(dst)[e] = reinterpret_cast<const uint16_t*>(sp)[e];
+          else
+            reinterpret_cast<uint32_t*>(dst)[e] = reinterpret_cast<const uint32_t*>(sp)[e];
+        }
+        __threadfence_block();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.bar[si]);
+      }
+    }
+    __syncwarp();
   };
 
   for (int b = static_cast<int>(cid); b < P.B; b += static_cast<int>(nC)) {
@@ -317,7 +418,9 @@ __global__ void __launch_bounds__(kTwThreads, 1) tree_walk_kernel(const TreeWalk
       sh.par[tid] = P.parent[static_cast<size_t>(b) * N + tid];
       sh.tok[tid] = P.tokens[static_cast<size_t>(b) * N + tid];
       sh.qr[tid] = P.q_row[static_cast<size_t>(b) * N + tid];
+      sh.ua[tid] = greedy ? 0.f : P.u_accept[static_cast<size_t>(b) * N + tid];
     }
+    if (tid == 0) sh.us = greedy ? 0.f : P.u_sample[b];
     if (tid == 0) {
       int e0 = 0;
       if (nn < 1 || nn > N || !(t >= 0.f) || tk < 0) e0 |= SV_DERR_ARG;
@@ -456,29 +559,33 @@ __global__ void __launch_bounds__(kTwThreads, 1) tree_walk_kernel(const TreeWalk
       // rows now and, prefetched, for the next step: the children's target
       // rows (and for MSS their children's draft rows)
       if (warp == 0) {
-        int prot[2 * kTwSlots];
-        int np = 0;
-        prot[np++] = key_of(0, node);
-        if (use_q && nc > 0) prot[np++] = key_of(1, sh.qr[sh.ch_list[c0]]);
+        int nw = 0, wkind = -1, wrow = -1;
+        auto want = [&](int kd, int rw) {
+          if (nw < kTwSlots) {
+            if (lane == nw) {
+              wkind = kd;
+              wrow = rw;
+            }
+            ++nw;
+          }
+        };
+        want(0, node);
+        if (use_q && nc > 0) want(1, sh.qr[sh.ch_list[c0]]);
         if (lane == 0) {
-          sh.ibuf[0] = prot[0];
-          sh.ibuf[1] = np > 1 ? prot[1] : prot[0];
+          sh.ibuf[0] = key_of(0, node);
+          sh.ibuf[1] = use_q && nc > 0 ? key_of(1, sh.qr[sh.ch_list[c0]]) : sh.ibuf[0];
         }
-        ensure(b, 0, node, prot, np);
-        if (use_q && nc > 0) ensure(b, 1, sh.qr[sh.ch_list[c0]], prot, np);
-        for (int k = 0; k < nc && np < kTwSlots; ++k) {
+        for (int k = 0; k < nc && nw < kTwSlots; ++k) {
           const int ch = sh.ch_list[c0 + k];
-          prot[np++] = key_of(0, ch);
-          ensure(b, 0, ch, prot, np);
+          want(0, ch);
           if (use_q) {
             const int g0 = sh.ch_start[ch], gn = sh.ch_start[ch + 1] - g0;
-            if (gn > 0 && np < kTwSlots) {
-              prot[np++] = key_of(1, sh.qr[sh.ch_list[g0]]);
-              ensure(b, 1, sh.qr[sh.ch_list[g0]], prot, np);
-            }
+            if (gn > 0) want(1, sh.qr[sh.ch_list[g0]]);
           }
         }
+        prefetch(b, nw, wkind, wrow);
       }
+      __syncthreads();  // the cache table, for acquire
       const unsigned char* prow = acquire(b, 0, node);
       if (greedy) {
         // ---- VerifyGreedy: the argmax of p_node (lowest id on ties)
@@ -545,9 +652,9 @@ __global__ void __launch_bounds__(kTwThreads, 1) tree_walk_kernel(const TreeWalk
         if (mloc[0] != kNegInf) sloc[0] += fast_exp2(scaled_arg(tw_elem<ES>(prow, e), mloc[0], c));
         if (qrow && mloc[1] != kNegInf) sloc[1] += fast_exp2(scaled_arg(tw_elem<ES>(qrow, e), mloc[1], c));
       }
-      const int fl0 = __syncthreads_or(bad) ? SV_DERR_NONFINITE : 0;
-      const MS bp = tw_block_ms(MS{mloc[0], sloc[0]}, c, sh);
-      const MS bq = qrow ? tw_block_ms(MS{mloc[1], sloc[1]}, c, sh) : MS{kNegInf, 0.f};
+      MS bp{mloc[0], sloc[0]}, bq{mloc[1], sloc[1]};
+      const int fl0 = tw_block_ms2(bp, bq, bad ? 1 : 0, c, sh) ? SV_DERR_NONFINITE : 0;
+      if (!qrow) bq = MS{kNegInf, 0.f};
       float gp = kNegInf, gq = kNegInf;
       int own = 0;
       if (nc > 0 && !naive) {
@@ -583,7 +690,7 @@ __global__ void __launch_bounds__(kTwThreads, 1) tree_walk_kernel(const TreeWalk
 
       if (naive) {
         // ---- naive sampling: x ~ p_node with the node's own uniform
-        const int x = draw(0, prow, nullptr, mp.m, P.u_accept[static_cast<size_t>(b) * N + node]);
+        const int x = draw(0, prow, nullptr, mp.m, sh.ua[node]);
         if (x < 0) {
           err |= SV_DERR_MASS;
           break;
@@ -605,7 +712,7 @@ __global__ void __launch_bounds__(kTwThreads, 1) tree_walk_kernel(const TreeWalk
       }
       if (nc == 0) {
         // ---- a leaf: the bonus token from p_node
-        token = draw(0, prow, nullptr, mp.m, P.u_sample[b]);
+        token = draw(0, prow, nullptr, mp.m, sh.us);
         if (token < 0) err |= SV_DERR_MASS;
         break;
       }
@@ -646,7 +753,7 @@ __global__ void __launch_bounds__(kTwThreads, 1) tree_walk_kernel(const TreeWalk
           // with (N, D) = (np, Zp) or (w, S).  First in fp32 with the
           // exponents as float pairs (about 5e-7 relative); calls closer than
           // 4e-6 relative, and exponents below -96, in fp64.
-          const float u32 = P.u_accept[static_cast<size_t>(b) * N + ch];
+          const float u32 = sh.ua[ch];
           float ahp = 0.f, ahq = 0.f;
           const float nq32 = removed ? 0.f : exp2_scaled_pair(gq, mq.m, c, ahq);
           const float num32 = rstate == 0 ? exp2_scaled_pair(gp, mp.m, c, ahp) : gp;
@@ -798,8 +905,8 @@ __global__ void __launch_bounds__(kTwThreads, 1) tree_walk_kernel(const TreeWalk
         continue;
       }
       // ---- every child rejected: the draw from r with u_sample
-      token = rstate == 0 ? draw(0, prow, nullptr, mp.m, P.u_sample[b])
-                          : draw(1, nullptr, cur ? wres1 : wres0, 0.f, P.u_sample[b]);
+      token = rstate == 0 ? draw(0, prow, nullptr, mp.m, sh.us)
+                          : draw(1, nullptr, cur ? wres1 : wres0, 0.f, sh.us);
       if (token < 0) err |= SV_DERR_MASS;
       break;
     }
