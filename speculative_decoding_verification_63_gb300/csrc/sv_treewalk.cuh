@@ -722,15 +722,33 @@ __global__ void __launch_bounds__(kTwThreads, 1) tree_walk_kernel(const TreeWalk
       int rstate = 0, cur = 0;
       double invS = 0.0;   // 1 / S in fp64 (thread 0: the accept tests)
       float finvS = 0.f;    // 1 / S in fp32 (every thread: the residual passes)
+      float Sres = 0.f;     // S, the residual's mass, in every thread
       int next = -1;
       int nq_id = qrow_id;        // the draft row whose statistics are in mq
       for (int k = 0; k < nc; ++k) {
         const int ch = sh.ch_list[c0 + k];
         const int x = sh.tok[ch];
         const int row_id = sh.qr[ch];
-        // the accept test, on one thread (fp64), handed to the block.
-        // Without replacement: q_j = q off the earlier siblings' (distinct)
-        // tokens, scaled by 1 / (1 - R), R their q mass.
+        // The accept test.  Every thread holds the same merged values, so
+        // every thread takes the same fp32 decision; the calls it leaves open
+        // (close ones, exponents below -96) and the rule without
+        // replacement after the first child (q_j = q off the earlier
+        // siblings' distinct tokens, scaled by 1 / (1 - R), R their q mass)
+        // go to thread 0, which decides them as below and hands the result
+        // to the block.
+        int acc = -1;
+        float fqs = 1.f;
+        if (!(P.mode == kTreeNoReplace && k > 0)) {
+          const float u32 = sh.ua[ch];
+          float ahp = 0.f, ahq = 0.f;
+          const float nq32 = exp2_scaled_pair(gq, mq.m, c, ahq);
+          const float num32 = rstate == 0 ? exp2_scaled_pair(gp, mp.m, c, ahp) : gp;
+          const float den32 = rstate == 0 ? mp.s : Sres;
+          const float lhs = u32 * nq32 * den32, rhs = num32 * mq.s;
+          if (ahp >= -96.f && ahq >= -96.f && fabsf(lhs - rhs) > 4e-6f * fmaxf(lhs, rhs))
+            acc = lhs < rhs;
+        }
+        if (acc < 0) {
         if (tid == 0) {
           double qs = 1.0;
           bool removed = false;
@@ -759,10 +777,10 @@ __global__ void __launch_bounds__(kTwThreads, 1) tree_walk_kernel(const TreeWalk
           const float num32 = rstate == 0 ? exp2_scaled_pair(gp, mp.m, c, ahp) : gp;
           const float den32 = rstate == 0 ? mp.s : sh.red[2][1];
           const float lhs = u32 * (nq32 * static_cast<float>(qs)) * den32, rhs = num32 * mq.s;
-          int acc;
+          int a0;
           if (ahp >= -96.f && ahq >= -96.f && qs == 1.0 &&
               fabsf(lhs - rhs) > 4e-6f * fmaxf(lhs, rhs)) {
-            acc = lhs < rhs;
+            a0 = lhs < rhs;
           } else {
             const double q = removed ? 0.0
                                      : exp2_nonpos((static_cast<double>(gq) - mq.m) * cd) /
@@ -771,15 +789,17 @@ __global__ void __launch_bounds__(kTwThreads, 1) tree_walk_kernel(const TreeWalk
                                  ? exp2_nonpos((static_cast<double>(gp) - mp.m) * cd) /
                                        static_cast<double>(mp.s)
                                  : static_cast<double>(gp) * invS;
-            acc = static_cast<double>(u32) * q < r;
+            a0 = static_cast<double>(u32) * q < r;
           }
-          sh.ibuf[2] = acc;
+          sh.ibuf[2] = a0;
           sh.red[2][0] = static_cast<float>(qs);
         }
         __syncthreads();
-        const bool accept = sh.ibuf[2] != 0;
-        const float fqs = sh.red[2][0];
+        acc = sh.ibuf[2];
+        fqs = sh.red[2][0];
         __syncthreads();
+        }
+        const bool accept = acc != 0;
         if (accept) {
           next = ch;
           break;
@@ -883,6 +903,7 @@ __global__ void __launch_bounds__(kTwThreads, 1) tree_walk_kernel(const TreeWalk
           rstate = 1;
           cur = nxt;
           finvS = rcp_fma(S);
+          Sres = S;
           if (tid == 0) {
             invS = 1.0 / static_cast<double>(S);
             sh.red[2][1] = S;  // read by thread 0 only (the next accept test)
