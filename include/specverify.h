@@ -26,8 +26,9 @@
  * (one per SM of the device) is resident at once, or the launch fails with
  * SV_ECORESIDENT.  A caller that confines the library to part of the GPU
  * (green contexts, MPS active-thread limits) gets that status rather than
- * timeouts.  The cluster kernels (trees, top-k rows) wait only inside a
- * cluster, which the hardware schedules as a unit.
+ * timeouts.  The tree walk and the row-statistics kernel wait only inside
+ * a thread-block cluster, which the hardware schedules as a unit; the
+ * top-k pass waits only within a CTA.
  *
  * Conventions for every entry point:
  *   - All array arguments are DEVICE pointers owned by the caller; the

@@ -125,3 +125,19 @@ def test_topk_above_host_bound_is_an_argument_error():
     n = out["out_len"].cpu().numpy()
     assert list(n[[1, 3]]) == [0, 0]
     assert np.all(n[[0, 2]] > 0)
+
+
+def test_topk_negative_and_narrow_rows():
+    """Rows whose logits are all negative (the row bound comes from the
+    coarse bins below zero) and rows packed into a narrow band far from zero
+    (many ties after bf16 rounding: the lists overflow and are cut exactly)."""
+    inp = wl.make_chain(5, B=6, V=40000, seed=wl.SEED_BASE + 507)
+    V = inp["V"]
+    rng = np.random.default_rng(13)
+    t = rng.normal(0, 3, (6, 9, V)).astype(np.float32)
+    t[0] = -30.0 + rng.normal(0, 5, (9, V)).astype(np.float32)      # all negative
+    t[1] = -1e4 + rng.normal(0, 50, (9, V)).astype(np.float32)       # far below zero
+    t[2] = 100.0 + rng.normal(0, 0.05, (9, V)).astype(np.float32)    # narrow band
+    t[3] = 0.0 + rng.normal(0, 1e-3, (9, V)).astype(np.float32)      # around zero
+    d = t[:, :8] + rng.normal(0, 0.5, (6, 8, V)).astype(np.float32)
+    check_chain(_rebuild(inp, t, d, 50))
