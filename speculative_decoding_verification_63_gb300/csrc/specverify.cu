@@ -29,7 +29,8 @@ struct Layout {
 };
 
 static_assert(kDrawTicketBase == SV_MAX_B, "draw tickets follow the request tickets");
-static_assert(kTkCap >= kTkStep + SV_MAX_TOPK, "after an exact cut a whole step fits the buffer");
+static_assert(static_cast<int64_t>(SV_MAX_V) / (kTkEpl * kTkMaxFold) * 4 <= kTkMapBytes,
+              "the top-k map holds a row of SV_MAX_V fp32 logits in groups of 16 kTkMaxFold");
 static_assert(sizeof(TopkShared) * kTkCtasPerSm + 2048 <= 228 * 1024,
               "the top-k pass keeps kTkCtasPerSm CTAs on an SM");
 static_assert(2 * SV_MAX_K + 1 <= 96, "top-k finalize: row statistics in three lanes' strides");
@@ -280,6 +281,15 @@ sv_status run_topk_pass(const sv_chain_args* a, void* workspace, const Layout& L
   t.es = es;
   t.max_topk = a->max_top_k;
   t.seg_len = TL.seg_len;
+  // the row's group maxima must fit one map of shared memory: groups of
+  // 16 f tokens, f doubled until they do (one key of es bytes per group)
+  t.fold = 1;
+  t.group_shift = 4;
+  while ((static_cast<int64_t>(a->V) + 16 * t.fold - 1) / (16 * t.fold) * es > kTkMapBytes) {
+    t.fold *= 2;
+    ++t.group_shift;
+  }
+  t.n_groups = static_cast<int>((static_cast<int64_t>(a->V) + 16 * t.fold - 1) / (16 * t.fold));
   t.has_draft = a->draft_logits != nullptr;
   t.target = static_cast<const char*>(a->target_logits);
   t.t_stride = a->target_row_stride * es;
@@ -522,8 +532,14 @@ sv_status sv_verify_chain(const sv_chain_args* a, void* workspace, size_t ws_byt
     if (ts != SV_OK) return ts;
   }
   // control CTAs (finalizes and draw finalizes, on SMs that stream nothing):
-  // one per 16 requests, 1 to 8; the rest of the grid streams
-  const int n_ctrl = static_cast<int>(std::min<int64_t>(8, std::max<int64_t>(1, (a->B + 15) / 16)));
+  // one per 16 requests, 1 to 8; the rest of the grid streams.  A call with
+  // top-k lists gets one per 4 requests, up to half the SMs: its filtered
+  // requests finalize from the lists alone, so their finalizes are all the
+  // work there is for them
+  const bool with_lists = a->top_k != nullptr && a->max_top_k > 0;
+  const int n_ctrl = static_cast<int>(
+      with_lists ? std::min<int64_t>(std::max(1, dev.sms / 2), std::max<int64_t>(1, (a->B + 3) / 4))
+                 : std::min<int64_t>(8, std::max<int64_t>(1, (a->B + 15) / 16)));
   const int64_t items_max = static_cast<int64_t>(a->B) * (2 * a->K + 1) * ipr;
   const int stream_ctas = static_cast<int>(
       std::min<int64_t>(std::max<int64_t>(items_max, 1), dev.sms - n_ctrl));

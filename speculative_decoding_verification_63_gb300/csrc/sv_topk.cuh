@@ -10,47 +10,54 @@
 // and the row's (m, Z) over them.  This pass produces exactly that, per
 // filtered row.
 //
-// A CTA takes one row at a time and moves on to the next; it has nine
+// A CTA takes one row at a time and moves on to the next; it has ten
 // warps.
 //
-//   stream  eight warps each read one eighth of the row (a segment) once,
-//           each lane keeping its candidates in its own list in shared
-//           memory (no warp-wide step to place them).
+//   stream  eight warps each read one eighth of the row (a segment) once.
 //           A streaming warp feeds itself: one lane keeps three 2 KB bulk
 //           copies of its segment in flight into a ring in shared memory,
 //           running on into the warp's segment of the next row, so the
 //           stream never waits out a memory latency at a row boundary.
-//           A token is kept only when its logit reaches the row's bound
-//           L: a value that at least k logits of the row reach, so that
-//           nothing below it can be in the top-k.  The eight warps raise L
-//           together.  Every kept logit is counted in a histogram of the
-//           row that the CTA shares (1/8-binade bins for positive logits,
-//           32 coarse bins below zero), and L is the lower edge of
-//           the highest bin at and above which k logits have been counted;
-//           a warp that finds a better L publishes it for the others.
-//           After the first few thousand tokens L sits just below the
-//           row's k-th best logit and most steps of 512 tokens keep
-//           nothing.  A buffer that fills (L held low by ties or by a
-//           narrow spread of logits) is first cleared of entries below L,
-//           then cut to its exact top-k; from then on the warp keeps only
-//           logits above the k-th best it holds (later tokens have higher
-//           ids, so an equal logit ranks below it).
-//   merge   the ninth warp concatenates the eight segment lists, cuts them
-//           to the row's exact top-k, sorts it into token order and writes
-//           the list and (m, Z), while the streaming warps go on to
-//           the next row.  Two sets of lists alternate between consecutive
-//           rows; named barriers hand a set from the streaming warps to the
-//           merging warp and back.
-//
-// Nothing is dropped that could be in the top-k: an entry leaves a buffer
-// only when it is below L or when k entries held rank above it.
+//           A step is 512 tokens, 16 consecutive tokens per lane.  The lane
+//           reduces its 16 logits to their maximum; the maximum of each
+//           group of 16 f consecutive tokens (f lanes; f = 1 unless the
+//           row's groups would not fit in shared memory) goes into the
+//           row's map, one order-preserving key per group, and the lane
+//           that leads a group keeps the largest key it wrote.  That is all
+//           a step does: no threshold to compare against and no branch on
+//           the data, so the pass streams at the speed of the copies.
+//   merge   two merging warps take turns, one per map: each takes the
+//           finished map of every other row while the streaming warps go on
+//           to the next (named barriers hand a map over and back), so a
+//           merge has the time of two rows.  Let T be the k-th largest group
+//           maximum.
+//           The row's top-k lies within k groups: every group whose maximum
+//           is above T (fewer than k), and of the groups whose maximum
+//           equals T the first ones in token order, as many as are missing
+//           to k.  (A kept logit in a group of maximum T equals T; each of
+//           the groups of maximum T before its own holds a logit equal to T
+//           with a lower id, and each group above T a logit above T: had
+//           its group been left out, k logits would rank above it.)  A
+//           first bound is the k-th largest of the lanes' keys: they are the
+//           maxima of 256 disjoint unions of groups, so at least k groups
+//           reach it.  One scan of the map collects the groups at or above
+//           it in token order, typically a few dozen, and T and the chosen
+//           groups follow from that short list: T by bisection on the key,
+//           then one pass that keeps the groups above T and the first ones
+//           equal to T.  A row with too many groups at
+//           the first bound (ties spread over the row) takes T by bisection
+//           over the whole map and the groups from a scan in token order.
+//           When f > 1 the warp re-reads the chosen groups and applies the same
+//           argument to their 16-token pieces.  It then reads the last k
+//           pieces (at most 16 k logits) into registers and finds their
+//           exact top-k: the k-th largest key K* by bisection, every logit
+//           above K*, and of those equal to K* the lowest ids.  The kept
+//           logits come out in token order, with (m, Z).
 //
 // Keys are order-preserving unsigned integers of the logit bits (16-bit
 // for bf16, 32-bit for fp32), 0 for NaN; -0 counts as +0, so equal logits
-// have equal keys.  An exact cut finds the k-th largest key K* by
-// narrowing histograms, keeps the keys above K*, and of the entries equal
-// to K* those with the lowest ids, up to k in all (found the same way, on
-// the ids).
+// have equal keys.  A row holding NaN or +inf gets an empty list and
+// (m, Z) = (NaN, 0).
 #pragma once
 
 #include "sv_rowpass.cuh"
@@ -58,25 +65,30 @@
 namespace sv {
 
 constexpr int kTkWarps = 8;                       // streaming warps, one segment of the row each
-constexpr int kTkThreads = (kTkWarps + 1) * 32;   // and the merging warp
+constexpr int kTkMergeWarps = 2;                  // merging warps, one per map parity
+constexpr int kTkThreads = (kTkWarps + kTkMergeWarps) * 32;
+constexpr int kTkBarCount = (kTkWarps + 1) * 32;  // threads on a hand-over barrier: the
+                                                  // streaming warps and one merging warp
 constexpr int kTkCtasPerSm = 2;                   // resident CTAs per SM (launch bounds)
-constexpr int kTkEpl = 16;                        // logits per lane per step
+constexpr int kTkEpl = 16;                        // consecutive logits per lane per step
 constexpr int kTkStep = 32 * kTkEpl;              // tokens per warp step
-constexpr int kTkCapLane = kTkEpl + (SV_MAX_TOPK + 31) / 32;  // a lane's list: a whole
-                                                  // step fits after an exact cut
-constexpr int kTkCap = 32 * kTkCapLane;           // candidates a streaming warp holds
 constexpr int kTkStageBytes = 2048;               // one bulk copy
 constexpr int kTkStages = 3;                      // bulk copies in flight per streaming warp
-constexpr int kTkSegAlign = 64;                   // segment starts: multiples of 64 tokens
-constexpr int kTkNegBins = 32;                    // row histogram: negative logits, coarse
-constexpr int kTkBins = kTkNegBins + 2048;        // and the rest in 1/8-binade bins
-// named barriers: + the set's parity, lists ready for the merge / set free
-// again; and the streaming warps among themselves
-constexpr uint32_t kTkBarFull = 1, kTkBarFree = 3, kTkBarStream = 5;
+constexpr int kTkMaxFold = 16;                    // lanes per group, at most
+constexpr int kTkSegAlign = kTkEpl * kTkMaxFold;  // segment starts: multiples of 256 tokens,
+                                                  // so no group straddles two segments
+constexpr int kTkMapBytes = 26624;                // one map: a 2- or 4-byte key per group
+constexpr int kTkSubCap = SV_MAX_TOPK * kTkMaxFold;  // pieces of the chosen groups
+constexpr int kTkListCap = kTkSubCap / 2;         // map entries at or above the first bound
+// named barriers: + the map's parity, map ready for the merge / map free
+constexpr uint32_t kTkBarFull = 1, kTkBarFree = 3;
 
 struct TopkPass {
   int n_req, K, V, es, max_topk;
   int seg_len;               // tokens per segment (multiple of kTkSegAlign); 8 segments cover V
+  int fold;                  // f: lanes per group (a power of two <= kTkMaxFold)
+  int group_shift;           // log2(16 f): token >> group_shift is the token's group
+  int n_groups;              // groups of the row, ceil(V / 16 f); n_groups * es <= kTkMapBytes
   bool bulk;                 // rows start 16-byte aligned, strides and V * es multiples of
                              // 16 bytes: segments stream through bulk copies
   bool has_draft;
@@ -94,21 +106,24 @@ struct TopkPass {
   int* err;                  // workspace error word (SV_DERR_TIMEOUT)
 };
 
-// Shared memory of one CTA (about 110 KB: two CTAs per SM).
+// A merging warp's scratch.
+struct TkMergeScratch {
+  alignas(16) unsigned sub[kTkSubCap];  // the map's entries at or above the first bound
+                                        // (keys, then indices), later the keys of the
+                                        // chosen groups' pieces
+  int pick[SV_MAX_TOPK];                // the chosen groups
+  int start[SV_MAX_TOPK];               // first tokens of the final pieces
+};
+
+// Shared memory of one CTA (about 113 KB: two CTAs per SM).
 struct TopkShared {
   unsigned char ring[kTkWarps][kTkStages][kTkStageBytes];  // bulk-copy rings
   uint64_t ring_bar[kTkWarps][kTkStages];
-  unsigned key[kTkWarps][kTkCap];        // streaming buffers
-  int id[kTkWarps][kTkCap];
-  unsigned cut_hist[kTkWarps + 1][256];  // scratch of each warp's exact cuts
-  unsigned row_hist[kTkBins];            // the row histogram
-  unsigned list_key[2][kTkWarps * SV_MAX_TOPK];  // per set: the segments' lists
-  int list_id[2][kTkWarps * SV_MAX_TOPK];
-  int list_cnt[2][kTkWarps];
-  unsigned bad[2];                       // per set: NaN or +inf seen in the row
-  unsigned top;                          // highest histogram bin with a count
-  unsigned count;                        // logits counted
-  unsigned row_lk;                       // the best bound found for the row (a key)
+  alignas(16) unsigned char map[2][kTkMapBytes];  // per parity: group maxima, zero padded
+                                                  // to a multiple of 16 bytes
+  unsigned lane_key[2][kTkWarps * 32];  // per parity: each lane's largest group key
+  TkMergeScratch ms[kTkMergeWarps];
+  unsigned bad[2];                      // per parity: NaN or +inf seen in the row
 };
 
 // Order-preserving keys.  bf16: x is the 16-bit pattern; fp32: the 32-bit
@@ -131,29 +146,6 @@ __device__ __forceinline__ float tk_value(unsigned key, int es) {
   }
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
 }
-__device__ __forceinline__ unsigned tk_key_of(float v, int es) {
-  return es == 2 ? tk_key16(__float_as_uint(v) >> 16) : tk_key32(__float_as_uint(v));
-}
-// Histogram bin of a key.  The bins that set L are those of the row's top
-// logits, which are positive in practice: a positive logit (or zero) gets
-// one of 2048 bins of 1/8 binade (its exponent and top three mantissa
-// bits); the negative logits share 32 coarse bins.  Monotone in the key.
-__device__ __forceinline__ unsigned tk_bin(unsigned key, int es) {
-  if (es == 2) return key < 0x8000u ? key >> 10 : kTkNegBins + ((key - 0x8000u) >> 4);
-  return key < 0x80000000u ? key >> 26 : kTkNegBins + ((key - 0x80000000u) >> 20);
-}
-// the lowest key of bin b
-__device__ __forceinline__ unsigned tk_bin_edge(unsigned b, int es) {
-  if (es == 2) return b < kTkNegBins ? b << 10 : 0x8000u + ((b - kTkNegBins) << 4);
-  return b < kTkNegBins ? b << 26 : 0x80000000u + ((b - kTkNegBins) << 20);
-}
-// the largest float below v (v > -inf, not NaN)
-__device__ __forceinline__ float tk_below(float v) {
-  const unsigned u = __float_as_uint(v);
-  if (v > 0.f) return __uint_as_float(u - 1u);
-  if (v == 0.f) return __uint_as_float(0x80000001u);
-  return __uint_as_float(u + 1u);
-}
 // NaN-propagating maximum
 __device__ __forceinline__ float fmax_nan(float a, float b) {
   float r;
@@ -161,460 +153,69 @@ __device__ __forceinline__ float fmax_nan(float a, float b) {
   return r;
 }
 
-// ---------------------------------------------------------------- lists
-//
-// A warp's candidates live in per-lane lists: lane l's i-th entry at index
-// l + 32 i of the warp's key / id arrays, i < c (the lane's count).  A
-// dense list of n entries is the case c = number of indices l + 32 i < n.
-// Entries are kept in no particular order: ties at the k-th value are
-// resolved by comparing ids.
+// ----------------------------------------------------------- the stream
 
-// lane l's count in a dense list of n entries
-__device__ __forceinline__ int tk_dense_count(int n, int lane) {
-  return n > lane ? (n - 1 - lane) / 32 + 1 : 0;
-}
-
-// Among the entries of the lists (rows = the largest count), the need-th
-// largest of the values that vof gives, over the entries it marks: returns
-// (that value V, how many marked entries have a value above V); need >= 1
-// and at most the number of marked entries.  V by narrowing a window of
-// values that holds it: starting from [min, max] of the marked values, a
-// 256-bin histogram of the window (bins 2^shift wide, so the window fills
-// the bins), walked down from the top bin until the running count reaches
-// the rank still wanted, fixes the bin that holds V; the next window is
-// that bin.  Lanes that hit the same bin add once (warp-aggregated).
-template <class F>
-__device__ __forceinline__ uint2 tk_select(F vof, int rows, int c, unsigned need,
-                                           unsigned* hist, int lane) {
-  unsigned mn = 0xffffffffu, mx = 0u;
-  for (int i = 0; i < rows; ++i) {
-    bool in = false;
-    unsigned v = 0u;
-    if (i < c) in = vof(i, v);
-    if (in) {
-      mn = min(mn, v);
-      mx = max(mx, v);
-    }
-  }
-  unsigned base = __reduce_min_sync(0xffffffffu, mn);
-  unsigned span = __reduce_max_sync(0xffffffffu, mx) - base;  // the window: [base, base + span]
-  unsigned above_all = 0u;
-  for (;;) {
-    const int shift = span < 256u ? 0 : 24 - __clz(span);  // (span >> shift) < 256
-#pragma unroll
-    for (int q = 0; q < 8; ++q) hist[lane * 8 + q] = 0u;
-    __syncwarp();
-    for (int i = 0; i < rows; ++i) {
-      bool in = false;
-      unsigned v = 0u;
-      if (i < c) in = vof(i, v);
-      in = in && v >= base && v - base <= span;
-      const unsigned bin = in ? (v - base) >> shift : 0u;
-      const unsigned m = __ballot_sync(0xffffffffu, in);
-      if (in) {
-        const unsigned peers = __match_any_sync(m, bin);
-        if (lane == __ffs(peers) - 1) atomicAdd(&hist[bin], static_cast<unsigned>(__popc(peers)));
-      }
-    }
-    __syncwarp();
-    // lane l holds bins 255 - 8 l .. 248 - 8 l (descending): lane order is
-    // bin order from the top
-    unsigned h[8], sum = 0u;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      h[q] = hist[255 - 8 * lane - q];
-      sum += h[q];
-    }
-    const unsigned incl = warp_incl_scan_u(sum, lane);
-    const unsigned owner = __ffs(__ballot_sync(0xffffffffu, incl >= need)) - 1;
-    int bin = 0;
-    unsigned above = 0u;
-    if (lane == static_cast<int>(owner)) {
-      unsigned cum = incl - sum;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        if (cum + h[q] >= need && cum < need) {
-          bin = 255 - 8 * lane - q;
-          above = cum;
-        }
-        cum += h[q];
-      }
-    }
-    bin = __shfl_sync(0xffffffffu, bin, owner);
-    above = __shfl_sync(0xffffffffu, above, owner);
-    need -= above;
-    above_all += above;
-    __syncwarp();
-    const unsigned lo = base + (static_cast<unsigned>(bin) << shift);
-    if (shift == 0) {
-      base = lo;
-      break;
-    }
-    span = min((1u << shift) - 1u, span - (static_cast<unsigned>(bin) << shift));
-    base = lo;
-  }
-  return make_uint2(base, above_all);
-}
-
-// Cut the lists (lane count c) to their exact top-k, written back dense:
-// the keys above K*, the k-th largest key, and of the keys equal to K*
-// those with the lowest ids.  Returns (entries kept, K*).  Lists of at most
-// k entries in all are only made dense (K* returned as 0, no key).
-__device__ __forceinline__ uint2 tk_cut(unsigned* key, int* id, unsigned* hist, int c, int k,
-                                     int lane) {
-  __syncwarp();
-  const int rows = static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(c)));
-  const unsigned total = __reduce_add_sync(0xffffffffu, static_cast<unsigned>(c));
-  const unsigned lt = (1u << lane) - 1u;
-  if (total <= static_cast<unsigned>(k)) {
-    unsigned written = 0u;
-    for (int i = 0; i < rows; ++i) {
-      const bool in = i < c;
-      const unsigned kk = in ? key[lane + 32 * i] : 0u;
-      const int ii = in ? id[lane + 32 * i] : 0;
-      const unsigned km = __ballot_sync(0xffffffffu, in);
-      __syncwarp();
-      if (in) {
-        const unsigned p = written + __popc(km & lt);
-        key[p] = kk;
-        id[p] = ii;
-      }
-      written += __popc(km);
-      __syncwarp();
-    }
-    return make_uint2(written, 0u);
-  }
-  const uint2 ks = tk_select(
-      [&](int i, unsigned& v) {
-        v = key[lane + 32 * i];
-        return true;
-      },
-      rows, c, static_cast<unsigned>(k), hist, lane);
-  const unsigned kstar = ks.x;
-  const unsigned need = static_cast<unsigned>(k) - ks.y;  // entries equal to K* to keep
-  unsigned ties = 0u;
-  for (int i = 0; i < c; ++i) ties += key[lane + 32 * i] == kstar ? 1u : 0u;
-  ties = __reduce_add_sync(0xffffffffu, ties);
-  // the ties kept: ids up to the need-th smallest (ids are distinct)
-  unsigned id_max = 0xffffffffu;
-  if (ties > need) {
-    const uint2 is = tk_select(
-        [&](int i, unsigned& v) {
-          v = 0xffffffffu - static_cast<unsigned>(id[lane + 32 * i]);
-          return key[lane + 32 * i] == kstar;
-        },
-        rows, c, need, hist, lane);
-    id_max = 0xffffffffu - is.x;
-  }
-  unsigned written = 0u;
-  for (int i = 0; i < rows; ++i) {
-    const bool in = i < c;
-    const unsigned kk = in ? key[lane + 32 * i] : 0u;
-    const int ii = in ? id[lane + 32 * i] : 0;
-    const bool keep = in && (kk > kstar || (kk == kstar && static_cast<unsigned>(ii) <= id_max));
-    const unsigned km = __ballot_sync(0xffffffffu, keep);
-    __syncwarp();  // row i is read before any of it is overwritten
-    if (keep) {
-      const unsigned p = written + __popc(km & lt);  // < 32 (i + 1): rows after i are untouched
-      key[p] = kk;
-      id[p] = ii;
-    }
-    written += __popc(km);
-    __syncwarp();
-  }
-  return make_uint2(written, kstar);
-}
-
-// Drop the lane's entries below key lk (in place); returns the lane's count.
-__device__ __forceinline__ int tk_compact(unsigned* key, int* id, int c, unsigned lk, int lane) {
-  int n = 0;
-  for (int i = 0; i < c; ++i) {
-    const unsigned kk = key[lane + 32 * i];
-    if (kk >= lk) {
-      id[lane + 32 * n] = id[lane + 32 * i];
-      key[lane + 32 * n] = kk;
-      ++n;
-    }
-  }
-  return n;
-}
-
-// A streaming warp's state for the row.  c is the lane's own count; the
-// rest is the same in every lane.
-struct TkWarp {
-  unsigned* key;  // per-lane lists
-  int* id;
-  unsigned* hist;  // scratch of the exact cut
-  int c;
-  unsigned hits;   // steps with a candidate, this row
-  unsigned lk;     // the row's bound L as a key; 0: none yet
-  unsigned thr;    // the k-th best key held at the warp's last exact cut; 0: none
-  float fv, eqv;   // the filter: keep logit x when x > fv or x == eqv
-};
-
-// The filter from L (keep x >= value(L)) and the warp's own k-th best
-// (keep x > value(thr)).  With neither, every non-NaN logit is kept.
-__device__ __forceinline__ void tk_filter(TkWarp& w, int es) {
-  const unsigned ninf = es == 2 ? 0x7fu : 0x7fffffu;  // the key of -inf
-  const float nan = __int_as_float(0x7fc00000);
-  w.fv = kNegInf;
-  w.eqv = kNegInf;
-  if (w.lk > ninf) {
-    w.fv = tk_below(tk_value(w.lk, es));
-    w.eqv = nan;
-  }
-  if (w.thr != 0u) {
-    const float t = tk_value(w.thr, es);
-    w.fv = w.eqv == w.eqv ? t : fmaxf(w.fv, t);
-    w.eqv = nan;
-  }
-}
-
-// The row's shared state: the histogram, its top bin, the logits counted
-// and the best bound any warp has found.
-struct TkRowState {
-  unsigned* hist;
-  unsigned* top;
-  unsigned* count;
-  unsigned* lk;
-};
-
-// Raise L.  The bound any warp found is read every time (one word); the
-// histogram is scanned on every fourth step with candidates: L is the lower
-// edge of the highest bin b with at least k logits counted at or above it.
-// Counts only grow and every counted logit is in the row, so the edge is a
-// valid bound whenever it is read.  A bound found is published for the
-// other warps.  Other warps move the shared words at any time: lane 0 reads
-// them once for the warp, so that every lane takes the same path.
-__device__ __forceinline__ void tk_refresh(TkWarp& w, const TkRowState& rs, bool scan, int k,
-                                           int es, int lane) {
-  unsigned n_seen = 0u, top_b = 0u, shared_lk = 0u;
-  if (lane == 0) {
-    shared_lk = *reinterpret_cast<volatile unsigned*>(rs.lk);
-    if (scan) {
-      n_seen = *reinterpret_cast<volatile unsigned*>(rs.count);
-      top_b = *reinterpret_cast<volatile unsigned*>(rs.top);
-    }
-  }
-  shared_lk = __shfl_sync(0xffffffffu, shared_lk, 0);
-  unsigned lk = max(w.lk, shared_lk);
-  if (scan) {
-    n_seen = __shfl_sync(0xffffffffu, n_seen, 0);
-    top_b = __shfl_sync(0xffffffffu, top_b, 0);
-    if (n_seen >= static_cast<unsigned>(k)) {
-      const int floor_b = static_cast<int>(tk_bin(lk, es));  // no gain at or below the bound's bin
-      const volatile unsigned* hist = rs.hist;
-      int hi = static_cast<int>(top_b);
-      unsigned carry = 0;
-      while (hi > floor_b) {
-        const int b = hi - lane;
-        const unsigned cb = b > floor_b ? hist[b] : 0u;
-        const unsigned incl = warp_incl_scan_u(cb, lane) + carry;
-        const unsigned hit =
-            __ballot_sync(0xffffffffu, b > floor_b && incl >= static_cast<unsigned>(k));
-        if (hit) {
-          lk = tk_bin_edge(static_cast<unsigned>(hi - (__ffs(hit) - 1)), es);
-          if (lane == 0) atomicMax(rs.lk, lk);
-          break;
-        }
-        carry = __shfl_sync(0xffffffffu, incl, 31);
-        hi -= 32;
-      }
-    }
-  }
-  if (lk != w.lk) {
-    w.lk = lk;
-    tk_filter(w, es);
-  }
-}
-
-// Layout of a step: lane l holds kTkEpl logits in G = ES groups of EPG =
-// 16 / ES consecutive tokens (16 bytes each); token of (g, l, j) =
-// g * 32 EPG + l * EPG + j.  Each group is one 16-byte load per lane, the
-// lanes' loads contiguous.
+// The maximum of a lane's 16 logits (ES 16-byte words), NaN-propagating.
 template <int ES>
-struct TkStep {
-  static constexpr int kEpg = 16 / ES;      // tokens per group per lane
-  static constexpr int kG = kTkEpl / kEpg;  // groups per step
-  static constexpr int kSpan = 32 * kEpg;   // tokens per group
-};
-
-// the bits of logit j of group words v (j warp-divergent): selects, no
-// local memory
-template <int ES>
-__device__ __forceinline__ unsigned tk_bits(const uint4& v, int j) {
+__device__ __forceinline__ float tk_piece_max(const uint4 (&raw)[ES]) {
   if constexpr (ES == 2) {
-    const unsigned a = (j & 2) ? v.y : v.x, b = (j & 2) ? v.w : v.z;
-    const unsigned word = (j & 4) ? b : a;
-    return (j & 1) ? (word >> 16) : (word & 0xffffu);
+    const unsigned w = bf16x2_max_nan(
+        bf16x2_max_nan(bf16x2_max_nan(raw[0].x, raw[0].y), bf16x2_max_nan(raw[0].z, raw[0].w)),
+        bf16x2_max_nan(bf16x2_max_nan(raw[1].x, raw[1].y), bf16x2_max_nan(raw[1].z, raw[1].w)));
+    return fmax_nan(bf16lo(w), bf16hi(w));
   } else {
-    const unsigned a = (j & 1) ? v.y : v.x, b = (j & 1) ? v.w : v.z;
-    return (j & 2) ? b : a;
-  }
-}
-// the key of a logit that passed the filter (never NaN)
-template <int ES>
-__device__ __forceinline__ unsigned tk_key_bits(unsigned x) {
-  if constexpr (ES == 2) {
-    if (x == 0x8000u) x = 0u;
-    return (x & 0x8000u) ? (~x & 0xffffu) : (x | 0x8000u);
-  } else {
-    if (x == 0x80000000u) x = 0u;
-    return (x & 0x80000000u) ? ~x : (x | 0x80000000u);
-  }
-}
-// logit j of group words v as a float (j a constant)
-template <int ES>
-__device__ __forceinline__ float tk_logit(const uint4& v, int j) {
-  const unsigned w4[4] = {v.x, v.y, v.z, v.w};
-  if constexpr (ES == 2) return (j & 1) ? bf16hi(w4[j >> 1]) : bf16lo(w4[j >> 1]);
-  else return __uint_as_float(w4[j]);
-}
-
-// The pass bits of one group (bit j: logit j of the lane's group passes).
-template <int ES>
-__device__ __forceinline__ unsigned tk_group_pass(const TkWarp& w, const uint4& v) {
-  constexpr int E = TkStep<ES>::kEpg;
-  unsigned pass = 0;
-  if (w.eqv == w.eqv) {  // no bound yet: every non-NaN logit
-#pragma unroll
-    for (int j = 0; j < E; ++j) {
-      const float x = tk_logit<ES>(v, j);
-      pass |= (x > w.fv || x == w.eqv) ? (1u << j) : 0u;
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < E; ++j) pass |= tk_logit<ES>(v, j) > w.fv ? (1u << j) : 0u;
-  }
-  return pass;
-}
-
-// The pass bits of a step, group g in bits g EPG ..; groups where no lane's
-// maximum mg[g] passes are skipped.
-template <int ES>
-__device__ __forceinline__ unsigned tk_step_pass(const TkWarp& w, const uint4 (&raw)[ES],
-                                                 const float (&mg)[ES], unsigned valid) {
-  using S = TkStep<ES>;
-  unsigned pass = 0;
-#pragma unroll
-  for (int g = 0; g < S::kG; ++g) {
-    const bool gh = !(mg[g] <= w.fv) || mg[g] == w.eqv;
-    if (__any_sync(0xffffffffu, gh)) pass |= tk_group_pass<ES>(w, raw[g]) << (g * S::kEpg);
-  }
-  return pass & valid;
-}
-
-// Keep the logits of one step (raw[g], the bits of `valid`; the step starts
-// at token id0) that pass the filter: each lane appends its own to its list
-// and counts them in the row histogram; then L is raised.  A full list is
-// first cleared of entries below L, and the warp's lists are cut to their
-// exact top-k if that is not enough.
-template <int ES>
-__device__ __forceinline__ void tk_take(TkWarp& w, const uint4 (&raw)[ES], unsigned valid,
-                                        const float (&mg)[ES], int id0, int k,
-                                        const TkRowState& rs, int lane) {
-  using S = TkStep<ES>;
-  unsigned pass = tk_step_pass<ES>(w, raw, mg, valid);
-  int cl = __popc(pass);
-  if (__any_sync(0xffffffffu, w.c + cl > kTkCapLane)) {
-    w.c = tk_compact(w.key, w.id, w.c, w.lk, lane);
-    if (__any_sync(0xffffffffu, w.c + cl > kTkCapLane)) {
-      // cut to the exact top-k (or, with at most k entries, spread evenly):
-      // at most 64 entries then, two per lane, so a whole step fits
-      const uint2 r = tk_cut(w.key, w.id, w.hist, w.c, k, lane);
-      w.c = tk_dense_count(static_cast<int>(r.x), lane);
-      if (r.y != 0u) {
-        w.thr = r.y;
-        tk_filter(w, ES);
-        pass = tk_step_pass<ES>(w, raw, mg, valid);
-        cl = __popc(pass);
-      }
-    }
-  }
-  if (cl) {
-    unsigned mb = 0u;
-    while (pass) {
-      const int i = __ffs(pass) - 1;
-      pass &= pass - 1u;
-      const int g = i / S::kEpg, j = i % S::kEpg;
-      uint4 v = raw[0];
-#pragma unroll
-      for (int q = 1; q < S::kG; ++q)
-        if (g == q) v = raw[q];
-      const unsigned kk = tk_key_bits<ES>(tk_bits<ES>(v, j));
-      w.key[lane + 32 * w.c] = kk;
-      w.id[lane + 32 * w.c] = id0 + g * S::kSpan + lane * S::kEpg + j;
-      ++w.c;
-      const unsigned b = tk_bin(kk, ES);
-      atomicAdd(rs.hist + b, 1u);
-      mb = max(mb, b);
-    }
-    atomicMax(rs.top, mb);
-    atomicAdd(rs.count, static_cast<unsigned>(cl));
-  }
-  __syncwarp();
-  ++w.hits;
-  tk_refresh(w, rs, (w.hits & 3u) == 1u, k, ES, lane);
-}
-
-// One step from its raw words (group g in raw[g]; logits beyond the segment
-// are -inf and left out of `valid`).  The NaN-propagating maxima tell
-// whether any logit can pass and, accumulated in mx, whether the row holds
-// NaN or +inf.
-template <int ES>
-__device__ __forceinline__ void tk_step(TkWarp& w, const uint4 (&raw)[ES], unsigned valid,
-                                        int id0, int k, const TkRowState& rs, float& mx,
-                                        int lane) {
-  float mg[ES];
-  if constexpr (ES == 2) {
-#pragma unroll
-    for (int g = 0; g < 2; ++g) {
-      const unsigned m2 = bf16x2_max_nan(bf16x2_max_nan(raw[g].x, raw[g].y),
-                                         bf16x2_max_nan(raw[g].z, raw[g].w));
-      mg[g] = fmax_nan(bf16lo(m2), bf16hi(m2));
-    }
-  } else {
+    float m[4];
 #pragma unroll
     for (int g = 0; g < 4; ++g)
-      mg[g] = fmax_nan(fmax_nan(__uint_as_float(raw[g].x), __uint_as_float(raw[g].y)),
-                       fmax_nan(__uint_as_float(raw[g].z), __uint_as_float(raw[g].w)));
+      m[g] = fmax_nan(fmax_nan(__uint_as_float(raw[g].x), __uint_as_float(raw[g].y)),
+                      fmax_nan(__uint_as_float(raw[g].z), __uint_as_float(raw[g].w)));
+    return fmax_nan(fmax_nan(m[0], m[1]), fmax_nan(m[2], m[3]));
   }
-  float m = mg[0];
-#pragma unroll
-  for (int g = 1; g < ES; ++g) m = fmax_nan(m, mg[g]);
-  mx = fmax_nan(mx, m);
-  const bool hit = !(m <= w.fv) || m == w.eqv;
-  if (!__any_sync(0xffffffffu, hit)) return;
-  tk_take<ES>(w, raw, valid, mg, id0, k, rs, lane);
 }
 
-// The logits of a step at and beyond `n` (segment-relative token `e0` of
-// the step's first logit) replaced by -inf, which leaves the step's maximum
-// to the tokens of the segment; returns the lane's valid bits.
+// One step: the lane's 16 logits raw (first token t = eb + 16 lane of the
+// segment, which holds n tokens and starts at token s0).  Folds the lane
+// maxima of each group, writes the group's key to the map and keeps the
+// lead lane's largest key.  Called by the whole warp.
 template <int ES>
-__device__ __forceinline__ unsigned tk_mask_tail(uint4 (&raw)[ES], int e0, int n, int lane) {
-  using S = TkStep<ES>;
-  unsigned valid = 0u;
+__device__ __forceinline__ void tk_step(const TopkPass& a, const uint4 (&raw)[ES], int eb, int n,
+                                        int s0, unsigned char* map, unsigned& lkey, float& mx,
+                                        int lane) {
+  const float m = tk_piece_max<ES>(raw);
+  mx = fmax_nan(mx, m);
+  unsigned key = ES == 2 ? tk_key16(__float_as_uint(m) >> 16) : tk_key32(__float_as_uint(m));
+  for (int o = 1; o < a.fold; o <<= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, o));
+  const int t = eb + kTkEpl * lane;
+  if ((lane & (a.fold - 1)) == 0 && t < n) {
+    const int g = (s0 + t) >> a.group_shift;
+    if constexpr (ES == 2) reinterpret_cast<unsigned short*>(map)[g] = static_cast<unsigned short>(key);
+    else reinterpret_cast<unsigned*>(map)[g] = key;
+    lkey = max(lkey, key);
+  }
+}
+
+// The lane's logits at and beyond segment token n replaced by -inf (t: the
+// segment token of the lane's first logit), which leaves the maximum to the
+// tokens of the segment.
+template <int ES>
+__device__ __forceinline__ void tk_mask_tail(uint4 (&raw)[ES], int t, int n) {
+  constexpr int E = 16 / ES;  // logits per word
 #pragma unroll
-  for (int g = 0; g < S::kG; ++g) {
-    const int t0 = e0 + g * S::kSpan + lane * S::kEpg;
+  for (int g = 0; g < ES; ++g) {
     unsigned v[4] = {raw[g].x, raw[g].y, raw[g].z, raw[g].w};
 #pragma unroll
-    for (int j = 0; j < S::kEpg; ++j) {
-      if (t0 + j >= n) {
+    for (int j = 0; j < E; ++j) {
+      if (t + g * E + j >= n) {
         if constexpr (ES == 2) {
           const int h = j >> 1;
           v[h] = (j & 1) ? ((v[h] & 0x0000ffffu) | 0xff800000u) : ((v[h] & 0xffff0000u) | 0xff80u);
         } else {
           v[j] = 0xff800000u;
         }
-      } else {
-        valid |= 1u << (g * S::kEpg + j);
       }
     }
     raw[g] = make_uint4(v[0], v[1], v[2], v[3]);
   }
-  return valid;
 }
 
 // the row of index r (b, i): target rows 0..nd, then the nd draft rows
@@ -676,120 +277,14 @@ __device__ __forceinline__ void tk_feed_issue(TkFeed& f, const TopkPass& a, int 
   }
 }
 
-// Sort 64 items (t = lane: (k0, i0); t = lane + 32: (k1, i1)) by id,
-// ascending, with a bitonic network.
-__device__ __forceinline__ void tk_cas(unsigned& kk, int& ii, int j, bool asc, int lane) {
-  const unsigned ko = __shfl_xor_sync(0xffffffffu, kk, j);
-  const int io = __shfl_xor_sync(0xffffffffu, ii, j);
-  const bool lower = (lane & j) == 0;
-  if (lower == asc ? io < ii : io > ii) {
-    kk = ko;
-    ii = io;
-  }
-}
-__device__ __forceinline__ void tk_sort64(unsigned& k0, int& i0, unsigned& k1, int& i1, int lane) {
-#pragma unroll
-  for (int size = 2; size <= 64; size <<= 1) {
-#pragma unroll
-    for (int j = size >> 1; j > 0; j >>= 1) {
-      if (j == 32) {
-        if (i1 < i0) {
-          const unsigned tk = k0;
-          const int ti = i0;
-          k0 = k1;
-          i0 = i1;
-          k1 = tk;
-          i1 = ti;
-        }
-      } else {
-        tk_cas(k0, i0, j, (lane & size) == 0, lane);
-        tk_cas(k1, i1, j, ((lane + 32) & size) == 0, lane);
-      }
-    }
-  }
-}
-
-// The merging warp: the row's exact top-k from the eight segment lists of
-// set p, written out in token order with (m, Z).  The lists are first packed
-// together in place.
-__device__ void tk_merge(const TopkPass& a, TopkShared& sh, int r, int p, int lane) {
-  const int R = 2 * a.K + 1;
-  const int b = r / R;
-  const int k = a.top_k[b];
-  unsigned* key = sh.list_key[p];
-  int* id = sh.list_id[p];
-  int cnt = 0;
-  for (int w = 0; w < kTkWarps; ++w) {
-    const int n = __shfl_sync(0xffffffffu, lane == 0 ? sh.list_cnt[p][w] : 0, 0);
-    for (int i0 = 0; i0 < n; i0 += 32) {
-      const int i = i0 + lane;
-      const unsigned kk = i < n ? key[w * SV_MAX_TOPK + i] : 0u;
-      const int ii = i < n ? id[w * SV_MAX_TOPK + i] : 0;
-      __syncwarp();  // read before any lane writes (the destination is never ahead)
-      if (i < n) {
-        key[cnt + i] = kk;
-        id[cnt + i] = ii;
-      }
-      __syncwarp();
-    }
-    cnt += n;
-  }
-  if (cnt > k)
-    cnt = static_cast<int>(
-        tk_cut(key, id, sh.cut_hist[kTkWarps], tk_dense_count(cnt, lane), k, lane).x);
-  __syncwarp();
-  unsigned k0 = lane < cnt ? key[lane] : 0u, k1 = lane + 32 < cnt ? key[lane + 32] : 0u;
-  int i0 = lane < cnt ? id[lane] : 0x7fffffff, i1 = lane + 32 < cnt ? id[lane + 32] : 0x7fffffff;
-  tk_sort64(k0, i0, k1, i1, lane);
-  const bool bad = __shfl_sync(0xffffffffu, lane == 0 ? sh.bad[p] : 0u, 0) != 0u;
-  float2* out = a.lists + static_cast<size_t>(r) * a.max_topk;
-  const float v0 = lane < cnt ? tk_value(k0, a.es) : kNegInf;
-  const float v1 = lane + 32 < cnt ? tk_value(k1, a.es) : kNegInf;
-  if (lane < k) out[lane] = make_float2(v0, __int_as_float(lane < cnt ? i0 : -1));
-  if (lane + 32 < k) out[lane + 32] = make_float2(v1, __int_as_float(lane + 32 < cnt ? i1 : -1));
-  float m = fmaxf(v0, v1);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  const Scale2 c = scale_for(a.temperature[b]);
-  float z = 0.f;
-  if (m != kNegInf) {
-    if (lane < cnt) z += fast_exp2(scaled_arg(v0, m, c));
-    if (lane + 32 < cnt) z += fast_exp2(scaled_arg(v1, m, c));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-  if (lane == 0) {
-    a.mz[r] = bad ? make_float2(__int_as_float(0x7fc00000), 0.f) : make_float2(m, z);
-    sh.bad[p] = 0u;
-  }
-  __syncwarp();
-}
-
-// the row's shared state cleared (each warp its eighth of the histogram)
-__device__ __forceinline__ void tk_clear_row(TopkShared& sh, int warp, int lane) {
-  for (int i = warp * (kTkBins / kTkWarps) + lane; i < (warp + 1) * (kTkBins / kTkWarps); i += 32)
-    sh.row_hist[i] = 0u;
-  if (warp == 0 && lane == 0) {
-    sh.top = 0u;
-    sh.count = 0u;
-    sh.row_lk = 0u;
-  }
-}
-
-// A streaming warp: its segment of every row the CTA takes.
+// A streaming warp: its segment of every row the CTA takes, into the map
+// of the row's parity.
 template <int ES>
 __device__ void tk_stream(const TopkPass& a, TopkShared& sh, int warp, int lane) {
-  using S = TkStep<ES>;
   const int n_rows = a.n_req * (2 * a.K + 1);
   const int G = static_cast<int>(gridDim.x);
   const int s0 = warp * a.seg_len;
   const int n = max(0, min(a.seg_len, a.V - s0));  // tokens of the segment (0: none)
-  TkWarp w;
-  w.key = sh.key[warp];
-  w.id = sh.id[warp];
-  w.hist = sh.cut_hist[warp];
-  const TkRowState rs{sh.row_hist, &sh.top, &sh.count, &sh.row_lk};
-  tk_clear_row(sh, warp, lane);
   TkFeed f;
   f.ring = &sh.ring[warp][0][0];
   f.bar = sh.ring_bar[warp];
@@ -814,17 +309,12 @@ __device__ void tk_stream(const TopkPass& a, TopkShared& sh, int warp, int lane)
     __syncwarp();
   }
   bool timed_out = false;
-  __syncwarp();
-  named_sync(kTkBarStream, kTkWarps * 32);
   int r = tk_next_row(a, static_cast<int>(blockIdx.x), G, n_rows);
   for (int p = 0; r < n_rows; p ^= 1) {
-    const int b = r / (2 * a.K + 1);
-    const int k = a.top_k[b];
-    w.c = 0;
-    w.hits = 0u;
-    w.lk = 0u;
-    w.thr = 0u;
-    tk_filter(w, ES);
+    // the merge is done with this parity's map (the row two back)
+    named_sync(kTkBarFree + p, kTkBarCount);
+    unsigned char* map = sh.map[p];
+    unsigned lkey = 0u;
     float mx = kNegInf;
     if (a.bulk) {
       for (int st = 0; st < f.n_stages; ++st) {
@@ -846,13 +336,11 @@ __device__ void tk_stream(const TopkPass& a, TopkShared& sh, int warp, int lane)
             const int eb = st * kStageEl + q * kTkStep;  // segment-relative
             if (eb >= n) break;                          // warp-uniform
             uint4 raw[ES];
+            const unsigned char* src = stage + (q * kTkStep + lane * kTkEpl) * ES;
 #pragma unroll
-            for (int g = 0; g < ES; ++g)
-              raw[g] = *reinterpret_cast<const uint4*>(stage + (q * kTkStep + g * S::kSpan) * ES +
-                                                       lane * 16);
-            const unsigned valid =
-                eb + kTkStep > n ? tk_mask_tail<ES>(raw, eb, n, lane) : 0xffffu;
-            tk_step<ES>(w, raw, valid, s0 + eb, k, rs, mx, lane);
+            for (int g = 0; g < ES; ++g) raw[g] = *reinterpret_cast<const uint4*>(src + 16 * g);
+            if (eb + kTkStep > n) tk_mask_tail<ES>(raw, eb + kTkEpl * lane, n);
+            tk_step<ES>(a, raw, eb, n, s0, map, lkey, mx, lane);
           }
         }
         __syncwarp();  // every lane is done with the slot
@@ -867,63 +355,34 @@ __device__ void tk_stream(const TopkPass& a, TopkShared& sh, int warp, int lane)
       // rows not fit for bulk copies: the same steps from plain loads
       const char* row = tk_row_ptr(a, r) + static_cast<int64_t>(s0) * ES;
       for (int eb = 0; eb < n; eb += kTkStep) {
+        const int t0 = eb + kTkEpl * lane;
+        unsigned v[4 * ES];
+#pragma unroll
+        for (int h = 0; h < 4 * ES; ++h) {
+          if constexpr (ES == 2) {
+            const int t = t0 + 2 * h;
+            const unsigned lo = t < n ? __ldg(reinterpret_cast<const unsigned short*>(row) + t)
+                                      : 0xff80u;
+            const unsigned hi = t + 1 < n
+                ? __ldg(reinterpret_cast<const unsigned short*>(row) + t + 1) : 0xff80u;
+            v[h] = lo | (hi << 16);
+          } else {
+            const int t = t0 + h;
+            v[h] = t < n ? __ldg(reinterpret_cast<const unsigned*>(row) + t) : 0xff800000u;
+          }
+        }
         uint4 raw[ES];
 #pragma unroll
-        for (int g = 0; g < ES; ++g) {
-          const int t0 = eb + g * S::kSpan + lane * S::kEpg;
-          unsigned v[4];
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            if constexpr (ES == 2) {
-              const int t = t0 + 2 * h;
-              const unsigned lo = t < n ? __ldg(reinterpret_cast<const unsigned short*>(row) + t)
-                                        : 0xff80u;
-              const unsigned hi = t + 1 < n
-                  ? __ldg(reinterpret_cast<const unsigned short*>(row) + t + 1) : 0xff80u;
-              v[h] = lo | (hi << 16);
-            } else {
-              const int t = t0 + h;
-              v[h] = t < n ? __ldg(reinterpret_cast<const unsigned*>(row) + t) : 0xff800000u;
-            }
-          }
-          raw[g] = make_uint4(v[0], v[1], v[2], v[3]);
-        }
-        unsigned valid = 0u;  // tokens of the segment
-#pragma unroll
-        for (int g = 0; g < S::kG; ++g)
-#pragma unroll
-          for (int j = 0; j < S::kEpg; ++j)
-            if (eb + g * S::kSpan + lane * S::kEpg + j < n) valid |= 1u << (g * S::kEpg + j);
-        tk_step<ES>(w, raw, valid, s0 + eb, k, rs, mx, lane);
+        for (int g = 0; g < ES; ++g)
+          raw[g] = make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+        tk_step<ES>(a, raw, eb, n, s0, map, lkey, mx, lane);
       }
     }
-    const bool bad = mx != mx || mx == kPosInf;
-    tk_refresh(w, rs, true, k, ES, lane);
-    w.c = tk_compact(w.key, w.id, w.c, w.lk, lane);
-    int total = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(w.c)));
-    if (total > k) {
-      total = static_cast<int>(tk_cut(w.key, w.id, w.hist, w.c, k, lane).x);
-      w.c = tk_dense_count(total, lane);
-    }
-    // hand the segment's list over (set p is free once the row two back is merged)
-    const unsigned incl = warp_incl_scan_u(static_cast<unsigned>(w.c), lane);
-    const int at = static_cast<int>(incl) - w.c;
-    __syncwarp();
-    named_sync(kTkBarFree + p, kTkThreads);
-    for (int i = 0; i < w.c; ++i) {
-      sh.list_key[p][warp * SV_MAX_TOPK + at + i] = w.key[lane + 32 * i];
-      sh.list_id[p][warp * SV_MAX_TOPK + at + i] = w.id[lane + 32 * i];
-    }
-    if (lane == 0) {
-      sh.list_cnt[p][warp] = total;
-      if (bad) sh.bad[p] = 1u;
-    }
-    named_arrive(kTkBarFull + p, kTkThreads);
-    // every streaming warp is done with the row's shared state: clear it
-    named_sync(kTkBarStream, kTkWarps * 32);
-    tk_clear_row(sh, warp, lane);
-    __syncwarp();
-    named_sync(kTkBarStream, kTkWarps * 32);
+    // hand the map over
+    sh.lane_key[p][warp * 32 + lane] = lkey;
+    const bool bad = __any_sync(0xffffffffu, mx != mx || mx == kPosInf);
+    if (bad && lane == 0) sh.bad[p] = 1u;
+    named_arrive(kTkBarFull + p, kTkBarCount);
     r = tk_next_row(a, r + G, G, n_rows);
   }
   // after a timeout, copies may still be in flight into the ring: wait for
@@ -939,6 +398,420 @@ __device__ void tk_stream(const TopkPass& a, TopkShared& sh, int warp, int lane)
   __syncwarp();
 }
 
+// ------------------------------------------------------------ the merge
+
+// key e of a 16-byte word of KB-byte keys
+template <int KB>
+__device__ __forceinline__ unsigned tk_word_key(const uint4& w, int e) {
+  if constexpr (KB == 2) {
+    const unsigned x = (e >> 1) == 0 ? w.x : (e >> 1) == 1 ? w.y : (e >> 1) == 2 ? w.z : w.w;
+    return (e & 1) ? (x >> 16) : (x & 0xffffu);
+  } else {
+    return e == 0 ? w.x : e == 1 ? w.y : e == 2 ? w.z : w.w;
+  }
+}
+
+// How many keys of an array of n16 16-byte words of KB-byte keys (zero
+// padded) are >= v (v >= 1).
+template <int KB>
+__device__ __forceinline__ unsigned tk_count_ge(const uint4* m, int n16, unsigned v, int lane) {
+  unsigned c = 0u;
+  if constexpr (KB == 2) {
+    const unsigned v2 = v | (v << 16);
+#pragma unroll 4
+    for (int i = lane; i < n16; i += 32) {
+      const uint4 w = m[i];
+      // 0xffff per half at or above v: 16 bits per key counted
+      c += __popc(__vcmpgeu2(w.x, v2)) + __popc(__vcmpgeu2(w.y, v2)) +
+           __popc(__vcmpgeu2(w.z, v2)) + __popc(__vcmpgeu2(w.w, v2));
+    }
+    c >>= 4;
+  } else {
+#pragma unroll 4
+    for (int i = lane; i < n16; i += 32) {
+      const uint4 w = m[i];
+      c += (w.x >= v ? 1u : 0u) + (w.y >= v ? 1u : 0u) + (w.z >= v ? 1u : 0u) +
+           (w.w >= v ? 1u : 0u);
+    }
+  }
+  return __reduce_add_sync(0xffffffffu, c);
+}
+
+// The largest key T with at least k keys >= T, by bisection from lo (at
+// least k keys reach it) and hi > lo (fewer than k reach it; n_hi of
+// them).  Returns (T, the number of keys above T).
+template <int KB>
+__device__ uint2 tk_kth(const uint4* m, int n16, int k, unsigned lo, unsigned hi, unsigned n_hi,
+                        int lane) {
+  while (hi - lo > 1u) {
+    const unsigned mid = lo + ((hi - lo) >> 1);
+    const unsigned c = tk_count_ge<KB>(m, n16, mid, lane);
+    if (c >= static_cast<unsigned>(k)) {
+      lo = mid;
+    } else {
+      hi = mid;
+      n_hi = c;
+    }
+  }
+  return make_uint2(lo, n_hi);
+}
+
+// The chosen entries of a key array, in index order: every key above T,
+// and of the keys equal to T the first `quota`.  Their indices go to
+// out[0 ..]; returns how many (at most cap; the scan stops there).
+template <int KB>
+__device__ int tk_pick(const uint4* m, int n16, unsigned T, int quota, int* out, int cap,
+                       int lane) {
+  constexpr int E = 16 / KB;  // keys per word
+  int written = 0, eq_seen = 0;
+  for (int i0 = 0; i0 < n16 && written < cap; i0 += 32) {
+    const int i = i0 + lane;
+    unsigned gt = 0u, eq = 0u;
+    if (i < n16) {
+      const uint4 w = m[i];
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const unsigned key = tk_word_key<KB>(w, e);
+        gt |= (key > T ? 1u : 0u) << e;
+        eq |= (key == T ? 1u : 0u) << e;
+      }
+    }
+    // the ties this lane may keep: the first (quota - ties before it)
+    const int ne = __popc(eq);
+    const int eq_incl = static_cast<int>(warp_incl_scan_u(static_cast<unsigned>(ne), lane));
+    const int room = quota - (eq_seen + eq_incl - ne);
+    unsigned eq_keep = eq;
+    for (int drop = ne - max(0, room); drop > 0; --drop) eq_keep &= ~(1u << (31 - __clz(eq_keep)));
+    const unsigned keep = gt | eq_keep;
+    const int nk = __popc(keep);
+    const int k_incl = static_cast<int>(warp_incl_scan_u(static_cast<unsigned>(nk), lane));
+    int at = written + k_incl - nk;
+    for (unsigned b = keep; b; b &= b - 1u, ++at)
+      if (at < cap) out[at] = i * E + (__ffs(b) - 1);
+    written += __shfl_sync(0xffffffffu, k_incl, 31);
+    eq_seen += __shfl_sync(0xffffffffu, eq_incl, 31);
+  }
+  __syncwarp();
+  return min(written, cap);
+}
+
+// The entries of a key array (n16 16-byte words of KB-byte keys) whose key
+// is at least lo, in index order: keys to key[], indices to idx[] (the
+// first kTkListCap of them).  Returns how many there are.  Few entries
+// reach the bound, so a word is mostly one test; a lane's place in the list
+// comes from ballots of the bits of its count (at most 8), no atomics.
+template <int KB>
+__device__ __forceinline__ int tk_collect(const uint4* m, int n16, unsigned lo, unsigned* key,
+                                          int* idx, int lane) {
+  constexpr int E = 16 / KB;  // keys per word
+  const unsigned lt = (1u << lane) - 1u;
+  int total = 0;
+#pragma unroll 2
+  for (int i0 = 0; i0 < n16; i0 += 32) {
+    const int i = i0 + lane;
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    unsigned hits = 0u;
+    if (i < n16) {
+      w = m[i];
+#pragma unroll
+      for (int e = 0; e < E; ++e) hits |= (tk_word_key<KB>(w, e) >= lo ? 1u : 0u) << e;
+    }
+    if (__any_sync(0xffffffffu, hits != 0u)) {
+      const unsigned c = static_cast<unsigned>(__popc(hits));
+      const unsigned b0 = __ballot_sync(0xffffffffu, c & 1u);
+      const unsigned b1 = __ballot_sync(0xffffffffu, c & 2u);
+      const unsigned b2 = __ballot_sync(0xffffffffu, c & 4u);
+      const unsigned b3 = __ballot_sync(0xffffffffu, c & 8u);
+      int at = total + __popc(b0 & lt) + 2 * __popc(b1 & lt) + 4 * __popc(b2 & lt) +
+               8 * __popc(b3 & lt);
+      for (; hits; hits &= hits - 1u, ++at) {
+        const int e = __ffs(hits) - 1;
+        if (at < kTkListCap) {
+          key[at] = tk_word_key<KB>(w, e);
+          idx[at] = i * E + e;
+        }
+      }
+      total += __popc(b0) + 2 * __popc(b1) + 4 * __popc(b2) + 8 * __popc(b3);
+    }
+  }
+  __syncwarp();
+  return total;
+}
+
+// The chosen groups from the list of the map's entries at or above lo
+// (keys key[], map indices idx[] ascending, n of them; at least k): with T
+// the k-th largest key, every entry above T and of those equal to T the
+// first ones, k in all, written to out[] in list order.  hi: above every
+// key.  Returns T.
+__device__ unsigned tk_pick_list(const unsigned* key, const int* idx, int n, int k, unsigned lo,
+                                 unsigned hi, int* out, int lane) {
+  unsigned n_hi = 0u;
+  while (hi - lo > 1u) {
+    const unsigned mid = lo + ((hi - lo) >> 1);
+    unsigned c = 0u;
+    for (int j = lane; j < n; j += 32) c += key[j] >= mid ? 1u : 0u;
+    c = __reduce_add_sync(0xffffffffu, c);
+    if (c >= static_cast<unsigned>(k)) {
+      lo = mid;
+    } else {
+      hi = mid;
+      n_hi = c;
+    }
+  }
+  const unsigned T = lo;
+  const int quota = k - static_cast<int>(n_hi);  // entries equal to T to keep
+  const unsigned lt = (1u << lane) - 1u;
+  int written = 0, ties = 0;
+  for (int j0 = 0; j0 < n; j0 += 32) {
+    const int j = j0 + lane;
+    const unsigned kj = j < n ? key[j] : 0u;
+    const bool tie = j < n && kj == T;
+    const unsigned bt = __ballot_sync(0xffffffffu, tie);
+    const bool keep = (j < n && kj > T) || (tie && ties + __popc(bt & lt) < quota);
+    const unsigned bk = __ballot_sync(0xffffffffu, keep);
+    if (keep && written + __popc(bk & lt) < k) out[written + __popc(bk & lt)] = idx[j];
+    written += __popc(bk);
+    ties += __popc(bt);
+  }
+  __syncwarp();
+  return T;
+}
+
+// The keys of the 16 logits from token t0 of a row (0 beyond V): vector
+// loads when the row is 16-byte aligned and the piece whole.
+template <int ES>
+__device__ __forceinline__ void tk_piece_keys(const char* row, int t0, int V, bool vec,
+                                              unsigned (&kk)[kTkEpl]) {
+  if (vec && t0 + kTkEpl <= V) {
+    const uint4* p = reinterpret_cast<const uint4*>(row + static_cast<int64_t>(t0) * ES);
+#pragma unroll
+    for (int g = 0; g < ES; ++g) {
+      const uint4 w = __ldg(p + g);
+      const unsigned x[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        if constexpr (ES == 2) {
+          kk[8 * g + 2 * h] = tk_key16(x[h] & 0xffffu);
+          kk[8 * g + 2 * h + 1] = tk_key16(x[h] >> 16);
+        } else {
+          kk[4 * g + h] = tk_key32(x[h]);
+        }
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kTkEpl; ++j) {
+      const int t = t0 + j;
+      if constexpr (ES == 2)
+        kk[j] = t < V ? tk_key16(__ldg(reinterpret_cast<const unsigned short*>(row) + t)) : 0u;
+      else
+        kk[j] = t < V ? tk_key32(__ldg(reinterpret_cast<const unsigned*>(row) + t)) : 0u;
+    }
+  }
+}
+
+// The exact top-k of the n (<= 64) 16-token pieces starting at tokens
+// start[0 ..] (ascending), written in token order to out with (m, Z).  lo:
+// a key that at least k of the pieces' logits reach.
+template <int ES>
+__device__ void tk_final(const TopkPass& a, const char* row, const int* start, int n, int k,
+                         unsigned lo, float temperature, float2* out, float2* mz, int lane) {
+  unsigned kk[2][kTkEpl];
+  int t0[2];
+  unsigned top = 0u;
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int i = lane + 32 * s;
+    t0[s] = i < n ? start[i] : -1;
+    if (t0[s] >= 0) {
+      tk_piece_keys<ES>(row, t0[s], a.V, a.bulk, kk[s]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < kTkEpl; ++j) kk[s][j] = 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < kTkEpl; ++j) top = max(top, kk[s][j]);
+  }
+  const unsigned hi0 = __reduce_max_sync(0xffffffffu, top) + 1u;
+  lo = max(lo, 1u);  // tokens beyond V (key 0) never count
+  if (lo >= hi0) lo = hi0 - 1u;
+  // K* = the k-th largest key, by bisection; n_gt keys above it
+  unsigned hi = hi0, n_gt = 0u;
+  while (hi - lo > 1u) {
+    const unsigned mid = lo + ((hi - lo) >> 1);
+    unsigned c = 0u;
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+#pragma unroll
+      for (int j = 0; j < kTkEpl; ++j) c += kk[s][j] >= mid ? 1u : 0u;
+    c = __reduce_add_sync(0xffffffffu, c);
+    if (c >= static_cast<unsigned>(k)) {
+      lo = mid;
+    } else {
+      hi = mid;
+      n_gt = c;
+    }
+  }
+  const unsigned kstar = lo;
+  const int quota = k - static_cast<int>(n_gt);  // logits equal to K* to keep
+  // keep masks per piece; ties counted in token order (pieces lane, then
+  // lane + 32)
+  unsigned gt[2], eq[2];
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    gt[s] = 0u;
+    eq[s] = 0u;
+#pragma unroll
+    for (int j = 0; j < kTkEpl; ++j) {
+      gt[s] |= (kk[s][j] > kstar && kstar >= 1u ? 1u : 0u) << j;
+      eq[s] |= (kk[s][j] == kstar && kstar >= 1u ? 1u : 0u) << j;
+    }
+  }
+  int tie_base = 0, out_base = 0;
+  unsigned keep[2];
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int ne = __popc(eq[s]);
+    const int eq_incl = static_cast<int>(warp_incl_scan_u(static_cast<unsigned>(ne), lane));
+    const int room = quota - (tie_base + eq_incl - ne);
+    unsigned ek = eq[s];
+    for (int drop = ne - max(0, room); drop > 0; --drop) ek &= ~(1u << (31 - __clz(ek)));
+    keep[s] = gt[s] | ek;
+    tie_base += __shfl_sync(0xffffffffu, eq_incl, 31);
+  }
+  // (m, Z): the largest key is kept whenever anything is
+  const float m = hi0 > 1u ? tk_value(hi0 - 1u, ES) : kNegInf;
+  const Scale2 c = scale_for(temperature);
+  float z = 0.f;
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int nk = __popc(keep[s]);
+    const int k_incl = static_cast<int>(warp_incl_scan_u(static_cast<unsigned>(nk), lane));
+    const int at0 = out_base + k_incl - nk;
+#pragma unroll
+    for (int j = 0; j < kTkEpl; ++j) {
+      if ((keep[s] >> j) & 1u) {
+        const int at = at0 + __popc(keep[s] & ((1u << j) - 1u));
+        const float v = tk_value(kk[s][j], ES);
+        if (at < k) out[at] = make_float2(v, __int_as_float(t0[s] + j));
+        if (m != kNegInf) z += fast_exp2(scaled_arg(v, m, c));
+      }
+    }
+    out_base += __shfl_sync(0xffffffffu, k_incl, 31);
+  }
+  for (int i = out_base + lane; i < k; i += 32) out[i] = make_float2(kNegInf, __int_as_float(-1));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  if (lane == 0) *mz = make_float2(m, z);
+  __syncwarp();
+}
+
+// The merging warp, row r from the map of parity p.  The map is released
+// (release: another row will use it) as soon as the groups are chosen.
+template <int ES>
+__device__ void tk_merge(const TopkPass& a, TopkShared& sh, TkMergeScratch& ms, int r, int p,
+                         bool release, int lane) {
+  const int R = 2 * a.K + 1;
+  const int b = r / R;
+  const int k = a.top_k[b];
+  const int f = a.fold;
+  const bool bad = __shfl_sync(0xffffffffu, lane == 0 ? sh.bad[p] : 0u, 0) != 0u;
+  int n_pick = 0;
+  unsigned T = 1u;
+  if (!bad) {
+    if (a.n_groups <= k) {
+      n_pick = a.n_groups;
+      for (int i = lane; i < n_pick; i += 32) ms.pick[i] = i;
+    } else {
+      // a first bound from the lanes' keys: their k-th largest
+      unsigned lk[8], mn = 0xffffffffu, mxk = 0u;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        lk[q] = sh.lane_key[p][8 * lane + q];
+        mn = min(mn, lk[q]);
+        mxk = max(mxk, lk[q]);
+      }
+      unsigned lo = __reduce_min_sync(0xffffffffu, mn);
+      unsigned hi = __reduce_max_sync(0xffffffffu, mxk) + 1u;
+      const unsigned top1 = hi;
+      while (hi - lo > 1u) {
+        const unsigned mid = lo + ((hi - lo) >> 1);
+        unsigned c = 0u;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) c += lk[q] >= mid ? 1u : 0u;
+        c = __reduce_add_sync(0xffffffffu, c);
+        if (c >= static_cast<unsigned>(k)) lo = mid;
+        else hi = mid;
+      }
+      // the map's entries at or above that bound: T and the chosen groups
+      // from them, unless there are too many (ties spread over the row):
+      // then by bisection over the whole map and a scan in token order
+      const uint4* map = reinterpret_cast<const uint4*>(sh.map[p]);
+      const int n16 = (a.n_groups * ES + 15) / 16;
+      unsigned* list_key = ms.sub;
+      int* list_idx = reinterpret_cast<int*>(ms.sub + kTkListCap);
+      const int n_c = lo >= 1u ? tk_collect<ES>(map, n16, lo, list_key, list_idx, lane) : 0;
+      if (lo >= 1u && n_c <= kTkListCap) {
+        T = tk_pick_list(list_key, list_idx, n_c, k, lo, top1, ms.pick, lane);
+        n_pick = k;
+      } else {
+        const uint2 t = tk_kth<ES>(map, n16, k, lo, top1, 0u, lane);
+        T = t.x;
+        n_pick = tk_pick<ES>(map, n16, t.x, k - static_cast<int>(t.y), ms.pick, k, lane);
+      }
+    }
+  }
+  __syncwarp();
+  if (lane == 0) sh.bad[p] = 0u;
+  if (release) named_arrive(kTkBarFree + p, kTkBarCount);
+
+  const char* row = tk_row_ptr(a, r);
+  float2* out = a.lists + static_cast<size_t>(r) * a.max_topk;
+  if (bad) {
+    for (int i = lane; i < k; i += 32) out[i] = make_float2(kNegInf, __int_as_float(-1));
+    if (lane == 0) a.mz[r] = make_float2(__int_as_float(0x7fc00000), 0.f);
+    __syncwarp();
+    return;
+  }
+  int n_start = n_pick;
+  if (f == 1) {
+    for (int i = lane; i < n_pick; i += 32) ms.start[i] = ms.pick[i] * kTkEpl;
+  } else {
+    // the chosen groups' 16-token pieces, in token order, and their keys
+    const int n_sub = n_pick * f;
+    const int n_sub4 = (n_sub + 3) & ~3;
+    unsigned top = 0u;
+    for (int s = lane; s < n_sub4; s += 32) {
+      unsigned key = 0u;
+      if (s < n_sub) {
+        unsigned kk[kTkEpl];
+        tk_piece_keys<ES>(row, (ms.pick[s / f] * f + s % f) * kTkEpl, a.V, a.bulk, kk);
+#pragma unroll
+        for (int j = 0; j < kTkEpl; ++j) key = max(key, kk[j]);
+      }
+      ms.sub[s] = key;
+      top = max(top, key);
+    }
+    __syncwarp();
+    if (n_sub <= k) {
+      n_start = n_sub;
+      for (int s = lane; s < n_sub; s += 32) ms.start[s] = s;
+    } else {
+      const uint4* sub = reinterpret_cast<const uint4*>(ms.sub);
+      const unsigned top1 = __reduce_max_sync(0xffffffffu, top) + 1u;
+      const uint2 t = tk_kth<4>(sub, n_sub4 / 4, k, max(T, 1u), top1, 0u, lane);
+      T = t.x;
+      n_start = tk_pick<4>(sub, n_sub4 / 4, t.x, k - static_cast<int>(t.y), ms.start, k, lane);
+    }
+    for (int i = lane; i < n_start; i += 32) {
+      const int s = ms.start[i];
+      ms.start[i] = (ms.pick[s / f] * f + s % f) * kTkEpl;
+    }
+  }
+  __syncwarp();
+  tk_final<ES>(a, row, ms.start, n_start, k, T, a.temperature[b], out, a.mz + r, lane);
+}
+
 __global__ void __launch_bounds__(kTkThreads, kTkCtasPerSm) topk_kernel(const TopkPass a) {
   extern __shared__ __align__(128) unsigned char tk_smem[];
   TopkShared& sh = *reinterpret_cast<TopkShared*>(tk_smem);
@@ -950,23 +823,27 @@ __global__ void __launch_bounds__(kTkThreads, kTkCtasPerSm) topk_kernel(const To
     else tk_stream<4>(a, sh, warp, lane);
     return;
   }
-  // the merging warp
+  // merging warp m takes the CTA's rows of parity m (every other row, from
+  // the m-th).  The padding of its map (never written by the stream) reads
+  // as key 0.
+  const int m = warp - kTkWarps;
   const int n_rows = a.n_req * (2 * a.K + 1);
   const int G = static_cast<int>(gridDim.x);
-  if (lane < 2) sh.bad[lane] = 0u;
+  const int used = a.n_groups * a.es;
+  for (int i = used + lane; i < ((used + 15) & ~15); i += 32) sh.map[m][i] = 0u;
+  if (lane == 0) sh.bad[m] = 0u;
+  auto next = [&](int x) { return x < n_rows ? tk_next_row(a, x + G, G, n_rows) : n_rows; };
   int r = tk_next_row(a, static_cast<int>(blockIdx.x), G, n_rows);
-  int r2 = r < n_rows ? tk_next_row(a, r + G, G, n_rows) : n_rows;
+  if (m == 1) r = next(r);
   __syncwarp();
-  if (r < n_rows) named_arrive(kTkBarFree + 0, kTkThreads);
-  if (r2 < n_rows) named_arrive(kTkBarFree + 1, kTkThreads);
-  for (int p = 0; r < n_rows; p ^= 1) {
+  if (r < n_rows) named_arrive(kTkBarFree + m, kTkBarCount);
+  while (r < n_rows) {
     __syncwarp();
-    named_sync(kTkBarFull + p, kTkThreads);
-    tk_merge(a, sh, r, p, lane);
-    const int r3 = r2 < n_rows ? tk_next_row(a, r2 + G, G, n_rows) : n_rows;
-    if (r3 < n_rows) named_arrive(kTkBarFree + p, kTkThreads);
-    r = r2;
-    r2 = r3;
+    named_sync(kTkBarFull + m, kTkBarCount);
+    const int rn = next(next(r));
+    if (a.es == 2) tk_merge<2>(a, sh, sh.ms[m], r, m, rn < n_rows, lane);
+    else tk_merge<4>(a, sh, sh.ms[m], r, m, rn < n_rows, lane);
+    r = rn;
   }
 }
 

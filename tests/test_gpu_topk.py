@@ -141,3 +141,22 @@ def test_topk_negative_and_narrow_rows():
     t[3] = 0.0 + rng.normal(0, 1e-3, (9, V)).astype(np.float32)      # around zero
     d = t[:, :8] + rng.normal(0, 0.5, (6, 8, V)).astype(np.float32)
     check_chain(_rebuild(inp, t, d, 50))
+
+
+@pytest.mark.parametrize("V,dt,K", [(262144, "bf16", 2), (600000, "bf16", 1), (131072, "fp32", 2)])
+def test_topk_large_vocab_folded_groups(V, dt, K):
+    """Vocabularies whose group maxima do not fit one map at 16 tokens per
+    group (groups of 32 or 64 tokens, re-read in 16-token pieces), with a
+    constant row (the k lowest ids) and rows of integer logits (ties at the
+    k-th value spread over many groups)."""
+    rng = np.random.default_rng(V)
+    B = 3
+    inp = wl.make_chain(5, B=B, K=K, V=V, seed=wl.SEED_BASE + 508)
+    inp["dtype"] = dt
+    t = rng.normal(0, 4, (B, K + 1, V)).astype(np.float32)
+    t[1] = 2.0
+    t[2] = np.round(rng.normal(0, 2, (K + 1, V))).astype(np.float32)
+    d = t[:, :K] + rng.normal(0, 2, (B, K, V)).astype(np.float32)
+    d[1] = 2.0
+    d[2] = np.round(d[2])
+    check_chain(_rebuild(inp, t, d, 50))
