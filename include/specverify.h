@@ -98,6 +98,9 @@ typedef enum {
 #define SV_DERR_TREE 0x08      /* parent / q_row / depth breaks the format */
 #define SV_DERR_TIMEOUT 0x10   /* a bounded wait on a bulk copy expired */
 #define SV_DERR_ARG 0x20       /* num_drafts, temperature or top_k invalid */
+#define SV_DERR_CHECK 0x40     /* an internal bounds or alignment check failed (debug
+                                  builds, -DSV_CHECKS, only): a library bug, never the
+                                  data; the access it guarded was skipped */
 
 /* Limits of this implementation. */
 #define SV_MAX_K 32        /* drafts per chain */

@@ -14,7 +14,7 @@ import threading
 import torch
 
 from ._binding import (  # noqa: F401
-    EXPORTS, SV_BF16, SV_DERR_ARG, SV_DERR_MASS, SV_DERR_NONFINITE, SV_DERR_TIMEOUT,
+    EXPORTS, SV_BF16, SV_DERR_ARG, SV_DERR_CHECK, SV_DERR_MASS, SV_DERR_NONFINITE, SV_DERR_TIMEOUT,
     SV_DERR_TOKEN, SV_DERR_TREE, SV_ECORESIDENT, SV_EDATA, SV_EINVAL, SV_ETIMEOUT, SV_EUNSUPPORTED,
     SV_EWORKSPACE, SV_FP32, SV_MAX_B, SV_MAX_K, SV_MAX_TOPK, SV_MAX_TREE_B,
     SV_MAX_TREE_NODES, SV_MAX_V, SV_OK, SpecVerifyError, lib, sv_chain_workspace_bytes,

@@ -20,6 +20,7 @@ SV_TREE_MSS, SV_TREE_MSS_NOREPLACE, SV_TREE_NAIVE = 0, 1, 2
 TREE_MODES = {"mss": SV_TREE_MSS, "noreplace": SV_TREE_MSS_NOREPLACE, "naive": SV_TREE_NAIVE}
 SV_DERR_TOKEN, SV_DERR_NONFINITE, SV_DERR_MASS = 0x01, 0x02, 0x04
 SV_DERR_TREE, SV_DERR_TIMEOUT, SV_DERR_ARG = 0x08, 0x10, 0x20
+SV_DERR_CHECK = 0x40
 SV_MAX_K, SV_MAX_B, SV_MAX_V, SV_MAX_TOPK = 32, 1024, 1 << 20, 64
 SV_MAX_TREE_NODES, SV_MAX_TREE_B = 64, 1024
 

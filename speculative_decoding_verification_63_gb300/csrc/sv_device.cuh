@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "specverify.h"
+
 namespace sv {
 
 constexpr float kPosInf = __builtin_huge_valf();
@@ -393,6 +395,26 @@ __device__ __forceinline__ DF warp_incl_scan_df(DF x, int lane) {
 }
 
 __device__ __forceinline__ void record_error(int* err, int flag) { atomicOr(err, flag); }
+
+// Internal checks of debug builds (-DSV_CHECKS): SV_CHECK(cond, err) is
+// true when cond holds; otherwise it sets SV_DERR_CHECK in the error word
+// *err and is false, and the caller skips the access it guards.  Release
+// builds compile every check to true.
+#ifdef SV_CHECKS
+__device__ __forceinline__ bool sv_check(bool ok, int* err) {
+  if (!ok) record_error(err, SV_DERR_CHECK);
+  return ok;
+}
+#define SV_CHECK(cond, err) ::sv::sv_check(static_cast<bool>(cond), (err))
+#else
+#define SV_CHECK(cond, err) true
+#endif
+// a 1-D bulk copy's requirements: both addresses 16-byte aligned, a size
+// that is a positive multiple of 16 bytes
+__device__ __forceinline__ bool bulk_args_ok(const void* dst, const void* src, uint32_t bytes) {
+  return ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src) | bytes) & 15u) == 0 &&
+         bytes > 0;
+}
 
 // Fetch-and-add with acquire-release semantics at GPU scope: orders this
 // thread's earlier stores before the add (release) and, for the thread that

@@ -181,6 +181,13 @@ __device__ void producer_loop(const P& prob, Shared& sh, const PosTables& tab,
       // one or two row pieces of n_el elements: [0, half) and [half, 2 half)
       const uint32_t bytes = static_cast<uint32_t>(m.n_el * prob.es);
       unsigned char* dst = stages + static_cast<size_t>(stage) * kChunkBytes;
+      if (!SV_CHECK(bulk_args_ok(dst, m.src, bytes) &&
+                        bytes <= static_cast<uint32_t>(m.src2 ? kChunkBytes / 2 : kChunkBytes) &&
+                        (m.src2 == nullptr || bulk_args_ok(dst + kChunkBytes / 2, m.src2, bytes)),
+                    err)) {
+        mbar_arrive(&sh.full[stage]);  // nothing copied: the stage completes empty
+        return;
+      }
       mbar_arrive_expect_tx(&sh.full[stage], m.src2 ? 2u * bytes : bytes);
       if (m.src2 == nullptr) {
         bulk_copy_g2s_hint(dst, m.src, bytes, &sh.full[stage], policy_evict_first());

@@ -188,6 +188,7 @@ __device__ __forceinline__ void tk_step(const TopkPass& a, const uint4 (&raw)[ES
   const int t = eb + kTkEpl * lane;
   if ((lane & (a.fold - 1)) == 0 && t < n) {
     const int g = (s0 + t) >> a.group_shift;
+    if (!SV_CHECK(g < a.n_groups, a.err)) return;
     if constexpr (ES == 2) reinterpret_cast<unsigned short*>(map)[g] = static_cast<unsigned short>(key);
     else reinterpret_cast<unsigned*>(map)[g] = key;
     lkey = max(lkey, key);
@@ -267,8 +268,14 @@ __device__ __forceinline__ void tk_feed_issue(TkFeed& f, const TopkPass& a, int 
   const int off = f.stage * kTkStageBytes;
   const uint32_t bytes = static_cast<uint32_t>(min(kTkStageBytes, f.seg_bytes - off));
   fence_proxy_async_shared();  // the slot's earlier reads before the copy's writes
-  mbar_arrive_expect_tx(&f.bar[slot], bytes);
-  bulk_copy_g2s_hint(f.ring + slot * kTkStageBytes, f.src + off, bytes, &f.bar[slot], f.pol);
+  if (SV_CHECK(bulk_args_ok(f.ring + slot * kTkStageBytes, f.src + off, bytes) &&
+                   off + static_cast<int>(bytes) <= f.seg_bytes,
+               a.err)) {
+    mbar_arrive_expect_tx(&f.bar[slot], bytes);
+    bulk_copy_g2s_hint(f.ring + slot * kTkStageBytes, f.src + off, bytes, &f.bar[slot], f.pol);
+  } else {
+    mbar_arrive(&f.bar[slot]);  // nothing copied: the stage completes empty
+  }
   ++f.issued;
   if (++f.stage == f.n_stages) {
     f.stage = 0;
@@ -623,6 +630,7 @@ __device__ void tk_final(const TopkPass& a, const char* row, const int* start, i
   for (int s = 0; s < 2; ++s) {
     const int i = lane + 32 * s;
     t0[s] = i < n ? start[i] : -1;
+    if (t0[s] >= 0 && !SV_CHECK(t0[s] < a.V && (t0[s] & (kTkEpl - 1)) == 0, a.err)) t0[s] = -1;
     if (t0[s] >= 0) {
       tk_piece_keys<ES>(row, t0[s], a.V, a.bulk, kk[s]);
     } else {

@@ -290,8 +290,13 @@ __global__ void __launch_bounds__(kTwThreads, 1) tree_walk_kernel(const TreeWalk
     if (P.bulk) {
       if (lane == 0) {
         const uint32_t bytes = static_cast<uint32_t>(n_sl * ES);
-        mbar_arrive_expect_tx(&sh.bar[s], bytes);
-        if (bytes > 0) bulk_copy_g2s_hint(dst, src, bytes, &sh.bar[s], pol);
+        if (bytes > 0 && !SV_CHECK(bulk_args_ok(dst, src, bytes) && bytes <= static_cast<uint32_t>(P.slot_bytes),
+                                   &P.hdr->error)) {
+          mbar_arrive(&sh.bar[s]);  // nothing copied: the slot completes empty
+        } else {
+          mbar_arrive_expect_tx(&sh.bar[s], bytes);
+          if (bytes > 0) bulk_copy_g2s_hint(dst, src, bytes, &sh.bar[s], pol);
+        }
       }
     } else {
       // rows unfit for bulk copies: the warp copies the slice
@@ -369,10 +374,14 @@ __global__ void __launch_bounds__(kTwThreads, 1) tree_walk_kernel(const TreeWalk
       sh.issued[slot] += 1u;
       if (P.bulk) {
         const uint32_t bytes = static_cast<uint32_t>(n_sl * ES);
-        mbar_arrive_expect_tx(&sh.bar[slot], bytes);
-        if (bytes > 0)
-          bulk_copy_g2s_hint(slots + static_cast<size_t>(slot) * P.slot_bytes, src, bytes,
-                             &sh.bar[slot], pol);
+        unsigned char* dst = slots + static_cast<size_t>(slot) * P.slot_bytes;
+        if (bytes > 0 && !SV_CHECK(bulk_args_ok(dst, src, bytes) && bytes <= static_cast<uint32_t>(P.slot_bytes),
+                                   &P.hdr->error)) {
+          mbar_arrive(&sh.bar[slot]);  // nothing copied: the slot completes empty
+        } else {
+          mbar_arrive_expect_tx(&sh.bar[slot], bytes);
+          if (bytes > 0) bulk_copy_g2s_hint(dst, src, bytes, &sh.bar[slot], pol);
+        }
       }
     }
     __syncwarp();

@@ -213,3 +213,22 @@ def test_nvtx_build_opens_a_range_per_entry_point():
                             *[f for f in _build.compile_flags() if f.startswith(("-I", "-D", "-std"))],
                             src], capture_output=True, text=True, check=True).stdout
     assert "SvRange" not in plain
+
+
+def test_checks_build_guards_the_bulk_copies():
+    """The debug build (-DSV_CHECKS) guards the bulk copies of the persistent
+    kernel, the top-k pass and the tree walk, and the top-k map and piece
+    indices, with checks that set SV_DERR_CHECK (preprocessed only: the
+    checks need no GPU); the release build has none of them."""
+    from speculative_decoding_verification_63_gb300 import _binding, _build
+    src = os.path.join(_build.CSRC, "specverify.cu")
+
+    def pre(checks):
+        flags = [f for f in _build.compile_flags(checks=checks) if f.startswith(("-I", "-D", "-std"))]
+        return subprocess.run([_build.nvcc(), "-E", "-x", "cu", *flags, src], capture_output=True,
+                              text=True, check=True).stdout
+    debug, release = pre(True), pre(False)
+    n_checks = debug.count("::sv::sv_check(")
+    assert n_checks >= 6, n_checks
+    assert "::sv::sv_check(" not in release
+    assert _binding.SV_DERR_CHECK == 0x40
