@@ -30,24 +30,23 @@
 //           finished map of every other row while the streaming warps go on
 //           to the next (named barriers hand a map over and back), so a
 //           merge has the time of two rows.  Let T be the k-th largest group
-//           maximum.
-//           The row's top-k lies within k groups: every group whose maximum
-//           is above T (fewer than k), and of the groups whose maximum
-//           equals T the first ones in token order, as many as are missing
-//           to k.  (A kept logit in a group of maximum T equals T; each of
-//           the groups of maximum T before its own holds a logit equal to T
-//           with a lower id, and each group above T a logit above T: had
-//           its group been left out, k logits would rank above it.)  A
-//           first bound is the k-th largest of the lanes' keys: they are the
-//           maxima of 256 disjoint unions of groups, so at least k groups
-//           reach it.  One scan of the map collects the groups at or above
-//           it in token order, typically a few dozen, and T and the chosen
-//           groups follow from that short list: T by bisection on the key,
-//           then one pass that keeps the groups above T and the first ones
-//           equal to T.  A row with too many groups at
-//           the first bound (ties spread over the row) takes T by bisection
-//           over the whole map and the groups from a scan in token order.
-//           When f > 1 the warp re-reads the chosen groups and applies the same
+//           maximum.  The row's top-k lies within k groups: every group
+//           whose maximum is above T (fewer than k), and of the groups whose
+//           maximum equals T the first ones in token order, as many as are
+//           missing to k.  (A kept logit in a group of maximum T equals T;
+//           each of the groups of maximum T before its own holds a logit
+//           equal to T with a lower id, and each group above T a logit
+//           above T: had its group been left out, k logits would rank above
+//           it.)  A first bound is the k-th largest of the lanes' keys: they
+//           are the maxima of 256 disjoint unions of groups, so at least k
+//           groups reach it.  One scan of the map collects the groups at or
+//           above it in token order, typically a few dozen, and T and the
+//           chosen groups follow from that short list: T by bisection on
+//           the key, then one pass that keeps the groups above T and the
+//           first ones equal to T.  A row with too many groups at the first
+//           bound (ties spread over the row) takes T by bisection over the
+//           whole map and the groups from a scan in token order.  When
+//           f > 1 the warp re-reads the chosen groups and applies the same
 //           argument to their 16-token pieces.  It then reads the last k
 //           pieces (at most 16 k logits) into registers and finds their
 //           exact top-k: the k-th largest key K* by bisection, every logit
