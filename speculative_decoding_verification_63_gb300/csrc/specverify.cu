@@ -532,14 +532,15 @@ sv_status sv_verify_chain(const sv_chain_args* a, void* workspace, size_t ws_byt
     if (ts != SV_OK) return ts;
   }
   // control CTAs (finalizes and draw finalizes, on SMs that stream nothing):
-  // one per 16 requests, 1 to 8; the rest of the grid streams.  A call with
+  // three per 32 requests, 1 to 8 (at B = 64, 6 of them gave the shortest
+  // step, 4 and 8 about 1.5 % longer); the rest of the grid streams.  A call with
   // top-k lists gets one per 4 requests, up to half the SMs: its filtered
   // requests finalize from the lists alone, so their finalizes are all the
   // work there is for them
   const bool with_lists = a->top_k != nullptr && a->max_top_k > 0;
   const int n_ctrl = static_cast<int>(
       with_lists ? std::min<int64_t>(std::max(1, dev.sms / 2), std::max<int64_t>(1, (a->B + 3) / 4))
-                 : std::min<int64_t>(8, std::max<int64_t>(1, (a->B + 15) / 16)));
+                 : std::min<int64_t>(8, std::max<int64_t>(1, (3 * a->B + 31) / 32)));
   const int64_t items_max = static_cast<int64_t>(a->B) * (2 * a->K + 1) * ipr;
   const int stream_ctas = static_cast<int>(
       std::min<int64_t>(std::max<int64_t>(items_max, 1), dev.sms - n_ctrl));
