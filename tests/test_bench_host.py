@@ -98,3 +98,11 @@ def test_cpu_oracle_one_thread_and_all_cores():
     import oracle
     want = oracle.verify_chain_inputs(wk.pool)
     assert np.array_equal(ref["out_tokens"], want["out_tokens"])
+
+
+def test_committed_dram_figures_match_the_current_sources():
+    """Each workload's committed ncu summary was taken on the kernel sources
+    as they are: bench.py finds its DRAM bytes (a stale summary gives null)."""
+    for key in (2, 3, 4, 5):
+        wk = bench.Workload(key)
+        assert bench.stored_traffic(wk.profile, wk.kernel), (wk.profile, wk.kernel)
